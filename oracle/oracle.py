@@ -1,0 +1,162 @@
+"""fp64 CPU oracle for packed-sequence attention and its fused Q/K prologue.
+
+TEST INFRASTRUCTURE.  Only the test suite, ``__graft_entry__.smoke()`` and
+``bench.py``'s CPU-baseline / reference leg may import or run this module.
+The CUDA product path never calls it and shares no code with it.
+
+What is computed, with the passage each step follows:
+
+* ``qk_norm_rope`` -- "QK normalization with partial RoPE", operator group 2
+  of Sol-H3 (arXiv 2609.35110) section 3.5 "Kernel Fusion", and the fused
+  Q/K RMSNorm + RoPE of the vLLM-Omni blog ("MiniMax H3 on vLLM-Omni"),
+  section 3.2 "fused DiT operators".  Per (row, head): RMSNorm over the
+  head's 128 channels with a per-head weight, eps inside the square root,
+  then an axial 3-D rotary embedding with sections (t, h, w) of widths
+  (32, 48, 48); channels past the rotary sections pass through.
+* ``attention`` -- exact softmax(Q K^T * scale) V per packed sequence or
+  query group and per head: the packed joint sequence and valid length of
+  the vLLM-Omni blog section 3.1 (the backend receives the valid length, the
+  suffix padding is removed), the flat (total, heads, head_dim) layout of
+  Sol-H3 section 3.2 "Optimized attention collectives", and the grouped
+  condition / audio / video query ranges of the SolarWM-H3 Realtime blog,
+  stage 2 "Attention Backend".
+
+Readings taken where the pages are silent (each listed in the design notes):
+RMSNorm per head (128 channels) with weight [H, 128]; eps inside the root;
+norm before rotation; rotary pairs are adjacent channels (2j, 2j+1) inside
+each section; pair j of a section of width d turns by pos * theta^(-2j/d);
+padded query rows and query rows with no valid key produce zeros.
+
+All arithmetic is float64 on exactly widened bf16 inputs; there is no
+intermediate rounding.  Matrix products and exp use NumPy as library
+primitives, with no blocking beyond splitting query rows into independent
+blocks (each output row depends on its own query row only).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+DEFAULT_SECTIONS = (32, 48, 48)
+DEFAULT_THETA = 10000.0
+DEFAULT_EPS = 1e-6
+
+
+def widen(t) -> np.ndarray:
+    """bf16 / fp32 tensor or array -> float64 ndarray (exact for bf16)."""
+    if isinstance(t, np.ndarray):
+        return t.astype(np.float64)
+    # torch tensor (any device); bf16 -> fp32 -> fp64 is exact.
+    return t.detach().to("cpu").float().numpy().astype(np.float64)
+
+
+# ---------------------------------------------------------------- prologue
+def rms_norm(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
+    """y_c = x_c / sqrt(mean_c(x_c^2) + eps) * w_c over the last axis."""
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + eps) * w
+
+
+def rope_inverse_frequencies(width: int, theta: float) -> np.ndarray:
+    """theta^(-2j/width) for the width/2 pairs of one axis section."""
+    j = np.arange(width // 2, dtype=np.float64)
+    return theta ** (-2.0 * j / width)
+
+
+def rope_axial(y: np.ndarray, pos: np.ndarray,
+               sections=DEFAULT_SECTIONS, theta=DEFAULT_THETA) -> np.ndarray:
+    """Rotate adjacent channel pairs of y [n, H, D] by per-axis angles.
+
+    Section a (t, h or w) covers channels [off_a, off_a + d_a); its pair j is
+    (off_a + 2j, off_a + 2j + 1) and turns by phi = pos[:, a] *
+    theta^(-2j/d_a):  (y0, y1) -> (y0 cos phi - y1 sin phi,
+    y0 sin phi + y1 cos phi).
+    """
+    out = y.copy()
+    off = 0
+    for a, d in enumerate(sections):
+        if d == 0:
+            continue
+        inv = rope_inverse_frequencies(d, theta)                # [d/2]
+        phi = pos[:, a].astype(np.float64)[:, None] * inv[None, :]
+        c = np.cos(phi)[:, None, :]                              # [n,1,d/2]
+        s = np.sin(phi)[:, None, :]
+        y0 = y[..., off:off + d:2]
+        y1 = y[..., off + 1:off + d:2]
+        out[..., off:off + d:2] = y0 * c - y1 * s
+        out[..., off + 1:off + d:2] = y0 * s + y1 * c
+        off += d
+    return out
+
+
+def qk_norm_rope(x: np.ndarray, w: np.ndarray, pos: np.ndarray,
+                 sections=DEFAULT_SECTIONS, theta=DEFAULT_THETA,
+                 eps=DEFAULT_EPS) -> np.ndarray:
+    """x [n, H, D] float64, w [H, D] float64, pos [n, 3] int -> [n, H, D]."""
+    assert sum(sections) <= x.shape[-1]
+    y = rms_norm(x, w[None, :, :], eps)
+    return rope_axial(y, pos, sections, theta)
+
+
+# --------------------------------------------------------------- attention
+def softmax_rows(s: np.ndarray) -> np.ndarray:
+    """Row-wise softmax of a float64 score block (max-subtracted)."""
+    m = np.max(s, axis=-1, keepdims=True)
+    e = np.exp(s - m)
+    return e / np.sum(e, axis=-1, keepdims=True)
+
+
+def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray,
+              cu_seqlens_q, cu_seqlens_kv, valid_len, scale: float,
+              rows=None, block: int = 256) -> np.ndarray:
+    """Non-causal attention per segment and head.
+
+    q [Rq, H, D], k / v [Rkv, H, D] float64.  Segment b owns query rows
+    [cu_q[b], cu_q[b+1]) and key rows [cu_kv[b], cu_kv[b+1]).  With
+    ``valid_len`` given, only the first valid_len[b] rows of each range are
+    valid (queries and keys alike); otherwise all rows are.  Output rows that
+    are padded, or whose segment has no valid key, are 0.
+
+    ``rows`` selects global query-row indices to compute (default: all);
+    the result has one output row per selected row, in that order.
+    """
+    Rq, H, D = q.shape
+    if rows is None:
+        rows = np.arange(Rq)
+    rows = np.asarray(rows, dtype=np.int64)
+    out = np.zeros((rows.size, H, D), dtype=np.float64)
+    n_seg = len(cu_seqlens_q) - 1
+    for b in range(n_seg):
+        q0, q1 = cu_seqlens_q[b], cu_seqlens_q[b + 1]
+        k0, k1 = cu_seqlens_kv[b], cu_seqlens_kv[b + 1]
+        nq, nkv = q1 - q0, k1 - k0
+        if valid_len is not None:
+            nq = nkv = valid_len[b]
+        sel = np.nonzero((rows >= q0) & (rows < q0 + nq))[0]
+        if sel.size == 0 or nkv == 0:
+            continue
+        for h in range(H):
+            kb = k[k0:k0 + nkv, h, :]
+            vb = v[k0:k0 + nkv, h, :]
+            for i in range(0, sel.size, block):
+                idx = sel[i:i + block]
+                s = scale * (q[rows[idx], h, :] @ kb.T)
+                out[idx, h, :] = softmax_rows(s) @ vb
+    return out
+
+
+def attention_flops(cu_seqlens_q, cu_seqlens_kv, valid_len, n_heads: int,
+                    head_dim: int, rows=None) -> float:
+    """Valid-token multiply-add count * 2 of the two products (4*H*D*Lq*Lkv),
+    restricted to ``rows`` when given."""
+    total = 0.0
+    for b in range(len(cu_seqlens_q) - 1):
+        q0, q1 = cu_seqlens_q[b], cu_seqlens_q[b + 1]
+        nq = q1 - q0
+        nkv = cu_seqlens_kv[b + 1] - cu_seqlens_kv[b]
+        if valid_len is not None:
+            nq = nkv = valid_len[b]
+        if rows is not None:
+            r = np.asarray(rows)
+            nq = int(np.count_nonzero((r >= q0) & (r < q0 + nq)))
+        total += 4.0 * n_heads * head_dim * nq * nkv
+    return total

@@ -1,0 +1,419 @@
+"""Pins of the fp64 oracle against facts fixed outside itself.
+
+Each check ties one part of the oracle to a closed form, an invariant, the
+independent pure-Python brute force, or a library routine (torch SDPA in
+float64 on the CPU), so that a plausible slip -- a dropped term, a wrong
+sign, a swapped index, a transposed operand, another rotary pairing -- fails
+at least one of them.  ``test_planted_mistakes_are_caught`` plants such
+slips in copies of the oracle and checks that the pins reject every one.
+"""
+import json
+import math
+import os
+import types
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import brute
+from oracle import oracle as O
+from packed_sequence_attention_gb300 import workloads as W
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SECTIONS = (32, 48, 48)
+THETA = 10000.0
+EPS = 1e-6
+SCALE = 1.0 / math.sqrt(128.0)
+
+
+def _tiny_inputs(fill="A"):
+    inp = W.make_inputs("tiny", fill=fill)
+    return inp, {k: O.widen(inp[k]) for k in ("q", "k", "v", "wq", "wk")}
+
+
+def _prologued_tiny(Ox=O, fill="A"):
+    inp, f = _tiny_inputs(fill)
+    pos = inp["pos_thw"].numpy()
+    q = Ox.qk_norm_rope(f["q"], f["wq"], pos, SECTIONS, THETA, EPS)
+    k = Ox.qk_norm_rope(f["k"], f["wk"], pos, SECTIONS, THETA, EPS)
+    return inp, q, k, f["v"]
+
+
+# ------------------------------------------------------------ pin checks
+# Each returns the worst deviation found; a pin holds when it is <= its bound.
+
+def pin_norm_closed_form(Ox):
+    """Unit weights: output mean square = ms / (ms + eps); explicit vector."""
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal((5, 3, 128)) * np.array([1e-3, 1.0, 30.0])[None, :, None]
+    y = Ox.rms_norm(x, np.ones(128), EPS)
+    ms = np.mean(x * x, -1)
+    dev = np.max(np.abs(np.mean(y * y, -1) - ms / (ms + EPS)) / (ms / (ms + EPS)))
+    # x = (3, 4, 0, ...): mean square 25/128, y = x / sqrt(25/128 + eps) * w
+    x1 = np.zeros(128); x1[0], x1[1] = 3.0, 4.0
+    w1 = np.linspace(0.5, 1.5, 128)
+    y1 = Ox.rms_norm(x1, w1, EPS)
+    r = 1.0 / math.sqrt(25.0 / 128.0 + EPS)
+    exp1 = np.zeros(128); exp1[0], exp1[1] = 3.0 * r * w1[0], 4.0 * r * w1[1]
+    return max(dev, float(np.max(np.abs(y1 - exp1))))
+
+
+def pin_norm_scale_invariance(Ox):
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal((7, 2, 128))
+    w = rng.standard_normal(128)
+    return float(np.max(np.abs(Ox.rms_norm(37.5 * x, w, 0.0) - Ox.rms_norm(x, w, 0.0))))
+
+
+def pin_rope_closed_forms(Ox):
+    """Single nonzero pair -> the 2x2 rotation by pos * theta^(-2j/d) of its
+    own axis; pairs are adjacent channels; other channels untouched."""
+    worst = 0.0
+    cases = [  # (channel c0, pos (t,h,w), expected angle)
+        (0, (1, 0, 0), 1.0),                                   # t, j=0
+        (2, (1, 0, 0), THETA ** (-2.0 / 32)),                  # t, j=1
+        (30, (3, 0, 0), 3 * THETA ** (-30.0 / 32)),            # t, last pair
+        (32, (0, 1, 0), 1.0),                                  # h, j=0
+        (32, (5, 0, 7), 0.0),                                  # h ignores t, w
+        (78, (0, 2, 0), 2 * THETA ** (-46.0 / 48)),            # h, last pair
+        (80, (0, 0, 1), 1.0),                                  # w, j=0
+        (126, (0, 0, 3), 3 * THETA ** (-46.0 / 48)),           # w, last pair
+        (100, (9, 9, 0), 0.0),                                 # w ignores t, h
+    ]
+    for c0, p, ang in cases:
+        y = np.zeros((1, 1, 128)); y[0, 0, c0] = 0.6; y[0, 0, c0 + 1] = -0.8
+        out = Ox.rope_axial(y, np.array([p]), SECTIONS, THETA)[0, 0]
+        exp = np.zeros(128)
+        exp[c0] = 0.6 * math.cos(ang) + 0.8 * math.sin(ang)
+        exp[c0 + 1] = 0.6 * math.sin(ang) - 0.8 * math.cos(ang)
+        worst = max(worst, float(np.max(np.abs(out - exp))))
+    return worst
+
+
+def pin_rope_invariants(Ox):
+    """|R(p) y| = |y| per pair; R(0) = I; <R(p+s)q, R(p'+s)k> = <R(p)q, R(p')k>
+    for a shift s along each axis separately."""
+    rng = np.random.default_rng(3)
+    y = rng.standard_normal((6, 2, 128))
+    pos = rng.integers(0, 60, size=(6, 3))
+    r = Ox.rope_axial(y, pos, SECTIONS, THETA)
+    pair_norm = lambda a: a[..., 0::2] ** 2 + a[..., 1::2] ** 2
+    worst = float(np.max(np.abs(pair_norm(r) - pair_norm(y))))
+    worst = max(worst, float(np.max(np.abs(
+        Ox.rope_axial(y, np.zeros((6, 3), int), SECTIONS, THETA) - y))))
+    q = rng.standard_normal((1, 1, 128)); k = rng.standard_normal((1, 1, 128))
+    p, pp = np.array([[4, 7, 2]]), np.array([[11, 3, 19]])
+    base = float(np.sum(Ox.rope_axial(q, p, SECTIONS, THETA) *
+                        Ox.rope_axial(k, pp, SECTIONS, THETA)))
+    for axis in range(3):
+        s = np.zeros((1, 3), int); s[0, axis] = 13
+        sh = float(np.sum(Ox.rope_axial(q, p + s, SECTIONS, THETA) *
+                          Ox.rope_axial(k, pp + s, SECTIONS, THETA)))
+        worst = max(worst, abs(sh - base))
+    return worst
+
+
+def pin_prologue_brute(Ox):
+    """NumPy prologue == pure-Python brute force on tiny rows of each kind."""
+    inp, f = _tiny_inputs()
+    pos = inp["pos_thw"].numpy()
+    rows = [0, 1, 63, 64, 127, 128, 150, 191, 192, 220, 249]
+    worst = 0.0
+    for name, wname in (("q", "wq"), ("k", "wk")):
+        got = Ox.qk_norm_rope(f[name], f[wname], pos, SECTIONS, THETA, EPS)
+        for r in rows:
+            for h in range(2):
+                exp = brute.norm_rope_row(list(f[name][r, h]), list(f[wname][h]),
+                                          tuple(int(v) for v in pos[r]),
+                                          SECTIONS, THETA, EPS)
+                worst = max(worst, float(np.max(np.abs(got[r, h] - np.array(exp)))))
+    return worst
+
+
+def pin_attention_brute(Ox):
+    """NumPy attention == pure-Python brute force (tiny, sampled rows)."""
+    inp, q, k, v = _prologued_tiny(Ox)
+    cu, vl = inp["cu_seqlens_q"], inp["valid_len"]
+    rows = [0, 5, 64, 127, 128, 191, 192, 249]
+    got = Ox.attention(q, k, v, cu, cu, vl, SCALE, rows=rows)
+    worst = 0.0
+    n = vl[0]
+    for i, r in enumerate(rows):
+        for h in range(2):
+            exp = brute.attention_row(list(q[r, h]), [list(k[j, h]) for j in range(n)],
+                                      [list(v[j, h]) for j in range(n)], SCALE)
+            worst = max(worst, float(np.max(np.abs(got[i, h] - np.array(exp)))))
+    return worst
+
+
+def pin_attention_closed_forms(Ox):
+    rng = np.random.default_rng(4)
+    L, H, D = 37, 2, 128
+    q = rng.standard_normal((L, H, D)); k = rng.standard_normal((L, H, D))
+    v = rng.standard_normal((L, H, D))
+    cu = [0, L]
+    worst = 0.0
+    # one valid key -> o = v_0 on valid rows (valid_len 1 -> only row 0 valid)
+    o = Ox.attention(q, k, v, cu, cu, [1], SCALE)
+    worst = max(worst, float(np.max(np.abs(o[0] - v[0]))), float(np.max(np.abs(o[1:]))))
+    # all V rows equal c -> o = c
+    c = rng.standard_normal((1, H, D))
+    o = Ox.attention(q, k, np.repeat(c, L, 0), cu, cu, None, SCALE)
+    worst = max(worst, float(np.max(np.abs(o - c))))
+    # all K rows equal -> uniform weights -> o = mean(V)
+    o = Ox.attention(q, np.repeat(k[:1], L, 0), v, cu, cu, None, SCALE)
+    worst = max(worst, float(np.max(np.abs(o - v.mean(0, keepdims=True)))))
+    # Q = 0 -> o = mean(V over valid keys)
+    o = Ox.attention(np.zeros_like(q), k, v, cu, cu, [20], SCALE)
+    worst = max(worst, float(np.max(np.abs(o[:20] - v[:20].mean(0, keepdims=True)))))
+    # two keys with score gap g -> weights (1, e^-g)/(1 + e^-g), exact closed form
+    qq = np.zeros((1, 1, D)); qq[0, 0, 0] = 1.0
+    kk = np.zeros((2, 1, D)); kk[0, 0, 0] = 3.0 / SCALE; kk[1, 0, 0] = 1.0 / SCALE
+    vv = np.zeros((2, 1, D)); vv[0, 0, 5] = 1.0; vv[1, 0, 5] = -2.0
+    o = Ox.attention(qq, kk, vv, [0, 1], [0, 2], None, SCALE)
+    p0 = 1.0 / (1.0 + math.exp(-2.0))
+    worst = max(worst, abs(o[0, 0, 5] - (p0 - 2.0 * (1.0 - p0))))
+    return worst
+
+
+def pin_attention_sdpa(Ox):
+    """Library cross-check: torch SDPA in float64 on the CPU, per segment."""
+    inp, q, k, v = _prologued_tiny(Ox)
+    n = inp["valid_len"][0]
+    got = Ox.attention(q, k, v, inp["cu_seqlens_q"], inp["cu_seqlens_kv"],
+                       inp["valid_len"], SCALE)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a[:n].transpose(1, 0, 2)))[None]
+    ref = torch.nn.functional.scaled_dot_product_attention(t(q), t(k), t(v))
+    ref = ref[0].numpy().transpose(1, 0, 2)
+    return float(np.max(np.abs(got[:n] - ref)))
+
+
+def pin_attention_grouped_sdpa(Ox):
+    """Grouped query ranges with unequal KV extents vs SDPA per group."""
+    rng = np.random.default_rng(5)
+    H, D = 2, 128
+    cu_q, cu_kv = [0, 9, 40, 41], [0, 30, 33, 100]
+    q = rng.standard_normal((41, H, D)); k = rng.standard_normal((100, H, D))
+    v = rng.standard_normal((100, H, D))
+    got = Ox.attention(q, k, v, cu_q, cu_kv, None, 0.3)
+    worst = 0.0
+    for b in range(3):
+        t = lambda a, lo, hi: torch.from_numpy(np.ascontiguousarray(
+            a[lo:hi].transpose(1, 0, 2)))[None]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            t(q, cu_q[b], cu_q[b + 1]), t(k, cu_kv[b], cu_kv[b + 1]),
+            t(v, cu_kv[b], cu_kv[b + 1]), scale=0.3)[0].numpy().transpose(1, 0, 2)
+        worst = max(worst, float(np.max(np.abs(got[cu_q[b]:cu_q[b + 1]] - ref))))
+    return worst
+
+
+def pin_attention_invariants(Ox):
+    """Joint permutation of valid K/V rows changes nothing; padded-row
+    contents (including NaN / Inf) change nothing on valid rows; padded
+    output rows are 0."""
+    inp, q, k, v = _prologued_tiny(Ox)
+    cu, vl = inp["cu_seqlens_q"], inp["valid_len"]
+    n = vl[0]
+    base = Ox.attention(q, k, v, cu, cu, vl, SCALE)
+    perm = np.random.default_rng(6).permutation(n)
+    k2, v2 = k.copy(), v.copy()
+    k2[:n], v2[:n] = k[perm], v[perm]
+    worst = float(np.max(np.abs(Ox.attention(q, k2, v2, cu, cu, vl, SCALE) - base)))
+    k3, v3, q3 = k.copy(), v.copy(), q.copy()
+    for a in (q3, k3, v3):
+        a[n:] = np.nan
+        a[n::3] = np.inf
+    o3 = Ox.attention(q3, k3, v3, cu, cu, vl, SCALE)
+    diff = np.abs(o3[:n] - base[:n])
+    worst = max(worst, float(np.max(np.where(np.isfinite(diff), diff, np.inf))))
+    worst = max(worst, float(np.max(np.abs(base[n:]))))
+    return worst
+
+
+def pin_softmax_rows(Ox):
+    rng = np.random.default_rng(7)
+    s = rng.standard_normal((9, 300)) * 40.0
+    p = Ox.softmax_rows(s)
+    # rows sum to 1; ratios follow exp of score differences
+    worst = float(np.max(np.abs(p.sum(-1) - 1.0)))
+    ratio = np.log(p[:, 1] / p[:, 0]) - (s[:, 1] - s[:, 0])
+    return max(worst, float(np.max(np.abs(ratio))))
+
+
+PINS = [
+    (pin_norm_closed_form, 1e-12),
+    (pin_norm_scale_invariance, 1e-12),
+    (pin_rope_closed_forms, 1e-12),
+    (pin_rope_invariants, 1e-10),
+    (pin_prologue_brute, 1e-12),
+    (pin_attention_brute, 1e-12),
+    (pin_attention_closed_forms, 1e-12),
+    (pin_attention_sdpa, 1e-12),
+    (pin_attention_grouped_sdpa, 1e-12),
+    (pin_attention_invariants, 1e-12),
+    (pin_softmax_rows, 1e-9),
+]
+
+
+@pytest.mark.parametrize("pin,bound", PINS, ids=[p.__name__ for p, _ in PINS])
+def test_pin(pin, bound):
+    assert pin(O) <= bound
+
+
+# ---------------------------------------------------- planted mistakes
+def _mutant(**overrides):
+    ns = types.SimpleNamespace(**{n: getattr(O, n) for n in dir(O) if not n.startswith("__")})
+    for name, fn in overrides.items():
+        setattr(ns, name, fn)
+    # re-bind composite functions so they call the mutated parts
+    def qk_norm_rope(x, w, pos, sections=SECTIONS, theta=THETA, eps=EPS):
+        return ns.rope_axial(ns.rms_norm(x, w[None], eps), pos, sections, theta)
+
+    def attention(q, k, v, cu_q, cu_kv, vl, scale, rows=None, block=256):
+        if "attention" in overrides:
+            return overrides["attention"](q, k, v, cu_q, cu_kv, vl, scale, rows)
+        saved = O.softmax_rows
+        try:
+            O.softmax_rows = ns.softmax_rows
+            return O.attention(q, k, v, cu_q, cu_kv, vl, scale, rows, block)
+        finally:
+            O.softmax_rows = saved
+    if "qk_norm_rope" not in overrides:
+        ns.qk_norm_rope = qk_norm_rope
+    ns.attention = attention
+    return ns
+
+
+def _rope_sign_flip(y, pos, sections=SECTIONS, theta=THETA):
+    return O.rope_axial(y, -np.asarray(pos), sections, theta)
+
+
+def _rope_rotate_half(y, pos, sections=SECTIONS, theta=THETA):
+    out = y.copy(); off = 0
+    for a, d in enumerate(sections):
+        inv = O.rope_inverse_frequencies(d, theta)
+        phi = pos[:, a][:, None] * inv[None]
+        c, s = np.cos(phi)[:, None], np.sin(phi)[:, None]
+        y0, y1 = y[..., off:off + d // 2], y[..., off + d // 2:off + d]
+        out[..., off:off + d // 2] = y0 * c - y1 * s
+        out[..., off + d // 2:off + d] = y0 * s + y1 * c
+        off += d
+    return out
+
+
+def _rope_shared_base(y, pos, sections=SECTIONS, theta=THETA):
+    # frequencies from the full head width instead of each axis' own width
+    out = y.copy(); off = 0
+    for a, d in enumerate(sections):
+        j = np.arange(d // 2)
+        phi = pos[:, a][:, None] * (theta ** (-2.0 * j / 128.0))[None]
+        c, s = np.cos(phi)[:, None], np.sin(phi)[:, None]
+        y0, y1 = y[..., off:off + d:2], y[..., off + 1:off + d:2]
+        out[..., off:off + d:2] = y0 * c - y1 * s
+        out[..., off + 1:off + d:2] = y0 * s + y1 * c
+        off += d
+    return out
+
+
+def _rope_axis_swap(y, pos, sections=SECTIONS, theta=THETA):
+    return O.rope_axial(y, np.asarray(pos)[:, [1, 0, 2]], sections, theta)
+
+
+def _norm_eps_outside(x, w, eps):
+    return x / (np.sqrt(np.mean(x * x, -1, keepdims=True)) + eps) * w
+
+
+def _norm_no_weight(x, w, eps):
+    return O.rms_norm(x, np.ones_like(w), eps)
+
+
+def _norm_sum_not_mean(x, w, eps):
+    return x / np.sqrt(np.sum(x * x, -1, keepdims=True) + eps) * w
+
+
+def _softmax_no_norm(s):
+    return np.exp(s - np.max(s, -1, keepdims=True))
+
+
+def _attn_transposed(q, k, v, cu_q, cu_kv, vl, scale, rows=None):
+    # uses V^T-like mixing: weights over queries instead of keys
+    return O.attention(k, q, v, cu_kv, cu_q, vl, scale, rows)
+
+
+def _attn_no_scale(q, k, v, cu_q, cu_kv, vl, scale, rows=None):
+    return O.attention(q, k, v, cu_q, cu_kv, vl, 1.0, rows)
+
+
+def _attn_pad_keys(q, k, v, cu_q, cu_kv, vl, scale, rows=None):
+    # attends over the whole buffer, padded keys included
+    return O.attention(q, np.nan_to_num(k), np.nan_to_num(v), cu_q, cu_kv, None, scale, rows)
+
+
+MUTANTS = {
+    "rope_sign_flip": dict(rope_axial=_rope_sign_flip),
+    "rope_rotate_half": dict(rope_axial=_rope_rotate_half),
+    "rope_shared_base": dict(rope_axial=_rope_shared_base),
+    "rope_axis_swap": dict(rope_axial=_rope_axis_swap),
+    "norm_eps_outside": dict(rms_norm=_norm_eps_outside),
+    "norm_no_weight": dict(rms_norm=_norm_no_weight),
+    "norm_sum_not_mean": dict(rms_norm=_norm_sum_not_mean),
+    "softmax_no_norm": dict(softmax_rows=_softmax_no_norm),
+    "attn_transposed": dict(attention=_attn_transposed),
+    "attn_no_scale": dict(attention=_attn_no_scale),
+    "attn_pad_keys": dict(attention=_attn_pad_keys),
+}
+
+
+def _pins_pass(Ox):
+    for pin, bound in PINS:
+        try:
+            val = pin(Ox)
+        except Exception:
+            return False
+        if not (val <= bound):
+            return False
+    return True
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistakes_are_caught(name):
+    assert _pins_pass(_mutant()), "unmutated copy must pass"
+    assert not _pins_pass(_mutant(**MUTANTS[name])), f"mutant {name} slipped through"
+
+
+# ------------------------------------------------------ pages' own numbers
+def test_workload_shapes_match_pages():
+    g = json.load(open(os.path.join(HERE, "golden", "workload_shapes.json")))
+    full = W.workload("full")
+    assert full.segments[0].valid == g["packed_sequence"]["valid_tokens"]
+    assert full.segments[0].q_rows == g["packed_sequence"]["buffer_tokens"]
+    assert full.n_heads * full.head_dim == g["hidden_width"]["value"]
+    assert full.head_dim == g["projection_channels"]["value"]
+
+
+def test_workload_flops_and_bytes():
+    # 4 * H * D * L^2 over valid tokens
+    assert W.workload("full").attention_flops() == 4 * 42 * 128 * 58758 ** 2
+    assert abs(W.workload("grouped_chunk").attention_flops() - 7.255e12) / 7.255e12 < 1e-3
+    assert abs(W.workload("full").prologue_bytes() - 2.527e9) / 2.527e9 < 1e-3
+
+
+def test_positions_layout():
+    pos = W.positions(W.workload("tiny")).numpy()
+    # video grid (2, 8, 8) t-major, then audio (i,0,0), then text (i,0,0), pad 0
+    assert tuple(pos[0]) == (0, 0, 0) and tuple(pos[9]) == (0, 1, 1)
+    assert tuple(pos[127]) == (1, 7, 7)
+    assert tuple(pos[128]) == (0, 0, 0) and tuple(pos[191]) == (63, 0, 0)
+    assert tuple(pos[192]) == (0, 0, 0) and tuple(pos[249]) == (57, 0, 0)
+    assert (pos[250:] == 0).all()
+
+
+def test_inputs_deterministic_and_padded():
+    a = W.make_inputs("tiny")
+    b = W.make_inputs("tiny")
+    assert torch.equal(a["q"].view(torch.int16), b["q"].view(torch.int16))
+    c = W.make_inputs("tiny", fill="B")
+    assert torch.isnan(c["k"][250:].float()).any() and torch.isinf(c["v"][250:].float()).any()
+    assert torch.equal(a["q"][:250].view(torch.int16), c["q"][:250].view(torch.int16))
+    assert torch.isnan(a["out"].float()).all()
