@@ -1,0 +1,396 @@
+"""Benchmark of the packed-sequence attention hot path on GB300.
+
+One step = the whole hot path over one packed-sequence block: the fused
+Q/K RMSNorm + axial RoPE on the valid rows of every sequence, then attention
+over the valid rows.  The default workload is the 58,816-row buffer holding
+58,758 valid tokens, 42 heads x 128 channels (bf16).
+
+Printed (rank 0, one JSON line): attention TFLOP/s over valid tokens for the
+whole job (value), the same through the public API from pinned host buffers
+(e2e), the roofline of the attention kernel, the prologue's GB/s, sampled
+SM clocks, and the fp64 CPU oracle timed on a bounded sample (cpu_baseline).
+
+``--impl reference`` times the CPU oracle instead (rank 0 only).
+Multi-GPU runs are independent replicas (the method has no exchange step on
+one GPU); value then sums the units of all ranks over the slowest rank.
+"""
+import os
+
+os.environ.setdefault("OMP_NUM_THREADS", str(os.cpu_count() or 1))
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(os.cpu_count() or 1))
+
+import argparse  # noqa: E402
+import json  # noqa: E402
+import math  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOP/s (valid tokens) at 58,816-tok packed seq; % bf16 peak; prologue GB/s"
+ROT = (32, 48, 48)
+SCALE = 1.0 / math.sqrt(128.0)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return dict(hbm=p["hbm_gbs"], bf16=p["bf16_tflops"],
+                    bf16_sustained=p["bf16_tflops_sustained"], source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# -------------------------------------------------------------- the GPU arm
+def launches_per_step(w):
+    return (len([s for s in w.segments if s.n_valid_q() > 0]) if w.self_attention else 0) + 1
+
+
+def run_step(h3, g, w, ev=None):
+    """Prologue on each sequence's valid rows, then attention.  With ``ev``
+    (four events), records prologue and attention boundaries."""
+    if ev is not None:
+        ev[0].record()
+    if w.self_attention:
+        for b, s in enumerate(w.segments):
+            if s.n_valid_q():
+                r0 = g["cu_seqlens_q"][b]
+                h3.qk_norm_rope(g["q"][r0:], g["k"][r0:], g["wq"], g["wk"], g["pos_thw"][r0:],
+                                n_rows=s.n_valid_q(), rot=ROT)
+    if ev is not None:
+        ev[1].record()
+    h3.attention(g["q"], g["k"], g["v"], g["cu_seqlens_q"], g["cu_seqlens_kv"], g["valid_len"],
+                 SCALE, out=g["out"])
+    if ev is not None:
+        ev[2].record()
+
+
+def parity_gate(h3, W, O, w):
+    """Fail-closed check on the same build before any number is reported:
+    the tiny packed sequence against the fp64 oracle."""
+    inp = W.make_inputs("tiny", fill="B")
+    g = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
+    run_step(h3, g, W.workload("tiny"))
+    torch.cuda.synchronize()
+    n = inp["valid_len"][0]
+    pos = inp["pos_thw"].numpy()[:n]
+    q = O.qk_norm_rope(O.widen(inp["q"][:n]), O.widen(inp["wq"]), pos)
+    k = O.qk_norm_rope(O.widen(inp["k"][:n]), O.widen(inp["wk"]), pos)
+    ref = O.attention(q, k, O.widen(inp["v"][:n]), [0, n], [0, n], None, SCALE)
+    got = O.widen(g["out"])
+    err = float(np.abs(got[:n] - ref).max())
+    rel = float(np.linalg.norm(got[:n] - ref) / np.linalg.norm(ref))
+    ok = err <= 2e-2 and rel <= 5e-3 and bool((got[n:] == 0).all()) and h3.status_word() == 0
+    return ok, {"max_abs": err, "rel_l2": rel}
+
+
+def cpu_baseline(O, inp_cpu, w, n_heads_sample, n_rows_sample):
+    """The fp64 oracle as it stands, on a bounded sample: n_rows_sample
+    query rows of the first sequence x n_heads_sample heads, each against all
+    valid keys of its sequence (prologue of those keys included)."""
+    s = w.segments[0]
+    q0, kv0 = inp_cpu["cu_seqlens_q"][0], inp_cpu["cu_seqlens_kv"][0]
+    nq, nkv = s.n_valid_q(), s.n_valid_kv()
+    rows = np.linspace(0, nq - 1, n_rows_sample).astype(np.int64) + q0
+    rows_t = torch.as_tensor(rows)
+    t0 = time.perf_counter()
+    for h in range(n_heads_sample):
+        qs = O.widen(inp_cpu["q"][rows_t, h:h + 1])
+        kh = O.widen(inp_cpu["k"][kv0:kv0 + nkv, h:h + 1])
+        vh = O.widen(inp_cpu["v"][kv0:kv0 + nkv, h:h + 1])
+        if w.self_attention:
+            pos = inp_cpu["pos_thw"].numpy()
+            qs = O.qk_norm_rope(qs, O.widen(inp_cpu["wq"][h:h + 1]), pos[rows])
+            kh = O.qk_norm_rope(kh, O.widen(inp_cpu["wk"][h:h + 1]), pos[kv0:kv0 + nkv])
+        O.attention(qs, kh, vh, [0, len(rows)], [0, nkv], None, SCALE)
+    dt = time.perf_counter() - t0
+    flops = 4.0 * 128 * nkv * len(rows) * n_heads_sample
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{len(rows)} query rows x {n_heads_sample} heads of '{w.name}' against "
+                      f"all {nkv} valid keys (fp64 NumPy oracle incl. the K prologue), "
+                      f"{dt:.1f} s wall"}
+
+
+def bench_gpu(args):
+    import packed_sequence_attention_gb300 as h3
+    from packed_sequence_attention_gb300 import workloads as W
+    from oracle import oracle as O
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    h3.lib()
+    pk = peaks()
+    w = W.workload(args.config)
+
+    ok, parity = parity_gate(h3, W, O, w)
+    if not ok:
+        raise SystemExit(f"parity gate failed: {parity}; no number reported")
+
+    # ---- device-resident inputs (seeded, generated on the GPU)
+    g = W.make_inputs(w, device=f"cuda:{local}", seed=W.default_seed(w) + rank)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        run_step(h3, g, w)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_start.record(stream)
+        for i in range(args.steps):
+            run_step(h3, g, w, evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    ms_total = t_start.elapsed_time(t_end)
+    attn_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
+    pro_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs])) if w.self_attention else 0.0
+    status = h3.status_word()
+    if status:
+        raise SystemExit(f"device status word {status:#x} after the timed region")
+    if dist is not None:
+        t = torch.tensor([ms_total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    flops = w.attention_flops()
+    value = flops * world / (ms_step * 1e-3) / 1e12
+    attn_tflops = flops / (attn_ms * 1e-3) / 1e12
+    pro_gbs = w.prologue_bytes() / (pro_ms * 1e-3) / 1e9 if pro_ms > 0 else None
+
+    # ---- end to end through the public API, pinned host buffers
+    host = {k: (v.cpu().pin_memory() if torch.is_tensor(v) else v) for k, v in
+            W.make_inputs(w, device=f"cuda:{local}", seed=W.default_seed(w) + rank).items()}
+    out_host = torch.empty_like(host["out"]).pin_memory()
+    names = ["q", "k", "v", "wq", "wk"] + (["pos_thw"] if w.self_attention else [])
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for n in names:
+            g[n].copy_(host[n], non_blocking=True)
+        run_step(h3, g, w)
+        out_host.copy_(g["out"], non_blocking=True)
+
+    for _ in range(min(args.warmup, 2)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    e_steps = max(1, min(args.steps, 5))
+    if dist is not None:
+        dist.barrier()
+    e_start.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    e_ms = e_start.elapsed_time(e_end) / e_steps
+    if dist is not None:
+        t = torch.tensor([e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e_ms = float(t.item())
+    e2e_value = flops * world / (e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        dist.barrier()
+        dist.destroy_process_group()
+        return
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        fresh = W.make_inputs(w, device=f"cuda:{local}")  # unmodified inputs
+        inp_cpu = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in fresh.items()}
+        del fresh
+        cpu = cpu_baseline(O, inp_cpu, w, args.cpu_heads, args.cpu_rows)
+    traffic = committed_traffic(w)
+    peak = pk["bf16_sustained"]
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 Q/K/V, N(1,0.1) norm weights, garbage pads)",
+        "config": {"workload": w.name, "description": w.description,
+                   "valid_tokens": [s.n_valid_q() for s in w.segments],
+                   "buffer_rows": [s.q_rows for s in w.segments],
+                   "heads": w.n_heads, "head_dim": 128,
+                   "attention_flop_per_step": flops,
+                   "prologue_bytes_per_step": w.prologue_bytes(),
+                   "l2": "inputs larger than L2 (Q,K,V 632 MB each); no flush"
+                   if w.name == "full" else "no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "achieved": round(attn_tflops, 2),
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(attn_tflops / peak, 4),
+                     "frac_of_burst": round(attn_tflops / pk["bf16"], 4),
+                     "peak_source": f"{pk['source']} bf16 (sustained; burst {pk['bf16']})",
+                     "kernel": "attn_fwd_kernel", "traffic": traffic},
+        "attention_ms": round(attn_ms, 4),
+        "attention_tflops": round(attn_tflops, 2),
+        "prologue_us": round(pro_ms * 1e3, 2) if pro_ms else None,
+        "prologue_gbs": round(pro_gbs, 1) if pro_gbs else None,
+        "prologue_frac_hbm_measured": round(pro_gbs / pk["hbm"], 4) if pro_gbs else None,
+        "prologue_frac_8tbs": round(pro_gbs / 8000.0, 4) if pro_gbs else None,
+        "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 3)},
+        "gpu_launches": launches_per_step(w) * args.steps,
+        "clocks": clk.summary(),
+        "parity": dict(parity, passed=True),
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def committed_traffic(w):
+    """DRAM bytes per attention launch from the committed ncu summary, if it
+    was taken on this workload and on the current kernel source."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "attention_traffic.txt")
+    src = os.path.join(ROOT, "packed_sequence_attention_gb300", "csrc", "attention.cu")
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    for line in open(path):
+        if ":" in line and not line.startswith("#"):
+            a, b = line.split(":", 1)
+            kv[a.strip()] = b.strip()
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if kv.get("source_sha256_16") != digest or kv.get("workload") != w.name:
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# -------------------------------------------------------- the reference arm
+def bench_reference(args):
+    """The CPU oracle timed as the reference arm: each step is a bounded
+    sample (args.ref_rows query rows x args.ref_heads heads) of the workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from packed_sequence_attention_gb300 import workloads as W
+    from oracle import oracle as O
+    w = W.workload(args.config)
+    inp = W.make_inputs(w, device="cuda" if torch.cuda.is_available() else "cpu")
+    inp = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in inp.items()}
+    for _ in range(args.warmup):
+        cpu_baseline(O, inp, w, args.ref_heads, args.ref_rows)
+    vals, t0 = [], time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(O, inp, w, args.ref_heads, args.ref_rows))
+    dt = time.perf_counter() - t0
+    value = float(np.mean([v["value"] for v in vals]))
+    line = {
+        "metric": METRIC, "impl": "reference", "value": value, "unit": "TFLOP/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "heads": w.n_heads, "head_dim": 128},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": vals[-1]["sample"]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="h3", choices=["h3", "reference"])
+    ap.add_argument("--config", default="full")
+    ap.add_argument("--cpu-heads", type=int, default=8)
+    ap.add_argument("--cpu-rows", type=int, default=64)
+    ap.add_argument("--ref-heads", type=int, default=2)
+    ap.add_argument("--ref-rows", type=int, default=32)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,147 @@
+/*
+ * h3kern -- packed-sequence attention and its fused Q/K RMSNorm + axial RoPE
+ * prologue for one DiT block of the MiniMax-H3 joint audio/video model,
+ * hand-written for sm_103a (GB300).
+ *
+ * C ABI: plain pointers and sizes.  Every call is asynchronous on the
+ * caller's CUDA stream, allocates no device memory and holds no reference
+ * to the caller's buffers after it returns.  The caller owns all device
+ * buffers and the stream.
+ *
+ * Tensor layout ("flat (total, heads, head_dim)", Sol-H3 arXiv 2609.35110,
+ * section 3.2 "Optimized attention collectives"): a tensor is
+ * [rows, n_heads, 128] bf16 with the 128 channels of a head contiguous,
+ * heads 128 elements apart, and rows `row_stride` ELEMENTS apart
+ * (row_stride >= n_heads * 128), so that views into a packed
+ * [rows, 3, n_heads, 128] QKV buffer can be passed without a copy.
+ *
+ * Errors: arguments are checked on the host before any CUDA call; a failed
+ * check returns a negative status and launches nothing.  The library never
+ * aborts or exits.  The message of the last nonzero status of the calling
+ * thread is available from h3_last_error().
+ */
+#ifndef H3KERN_H
+#define H3KERN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* h3_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+enum {
+  H3_OK = 0,
+  H3_ERR_ARG = -1,     /* null pointer, bad count, non-finite scalar, bad cu_seqlens */
+  H3_ERR_ALIGN = -2,   /* base pointer or row stride not 16-byte aligned */
+  H3_ERR_SHAPE = -3,   /* head_dim != 128, row stride too small, bad rotary split */
+  H3_ERR_ARCH = -4,    /* current device is not compute capability 10.3 (sm_103) */
+  H3_ERR_LAUNCH = -5,  /* the kernel launch itself failed */
+  H3_ERR_TIMEOUT = -6, /* a bounded device-side wait gave up (see h3_status_word) */
+  H3_ERR_DEVICE = -7   /* CUDA runtime / driver error outside a launch */
+};
+
+/* Most segments (packed sequences or query groups) one h3_attention call takes. */
+#define H3_MAX_SEGMENTS 16
+
+/* Bits of the device status word (h3_status_word). */
+#define H3_STATUS_TIMEOUT_LOAD 0x1u   /* producer gave up waiting for a free K/V stage */
+#define H3_STATUS_TIMEOUT_MMA 0x2u    /* MMA issuer gave up waiting for data or P */
+#define H3_STATUS_TIMEOUT_SOFTMAX 0x4u/* softmax warps gave up waiting for S or O */
+#define H3_STATUS_ABORTED 0x8u        /* a CTA stopped early because another gave up */
+
+/*
+ * h3_qk_norm_rope -- fused Q/K RMSNorm + axial 3-D RoPE, in place, one pass.
+ *
+ * Follows "QK normalization with partial RoPE" (Sol-H3, section 3.5 "Kernel
+ * Fusion", operator group 2) and the fused Q/K RMSNorm + RoPE of the vLLM-Omni
+ * blog (section 3.2).  For every row r < n_rows and head h, with x the 128
+ * channels of q[r, h] (and likewise k[r, h] with wk):
+ *
+ *   y_c  = x_c / sqrt(mean_c(x_c^2) + eps) * w[h, c]            (fp32)
+ *   the channels are split into sections t = [0, rot_t),
+ *   h = [rot_t, rot_t + rot_h), w = [rot_t + rot_h, rot_t + rot_h + rot_w);
+ *   pair j of a section of width d is channels (off + 2j, off + 2j + 1),
+ *   turned by phi = pos_thw[r, a] * theta^(-2j/d):
+ *   (y0, y1) -> (y0 cos phi - y1 sin phi, y0 sin phi + y1 cos phi);
+ *   channels past rot_t + rot_h + rot_w are only normalised;
+ *   the result is rounded once to bf16 (round-to-nearest-even) and stored
+ *   over x.
+ *
+ * q, k        device bf16 [n_rows, n_heads, 128], row strides in elements;
+ *             modified in place; q and k must not overlap.
+ * wq, wk      device bf16 [n_heads, 128], per-head norm weights.
+ * pos_thw     device int32 [n_rows, 3]: (t, h, w) position of each row.
+ * n_rows      rows to process (0 = nothing to do); typically the valid rows.
+ * head_dim    must be 128.
+ * rot_t/h/w   even, >= 0, rot_t + rot_h + rot_w <= 128 (the configs use 32/48/48).
+ * theta       RoPE base (> 0, finite); eps >= 0, finite.
+ * Alignment:  q, k, wq, wk 16-byte aligned; row strides * 2 bytes a multiple of 16;
+ *             pos_thw 4-byte aligned.
+ * Returns H3_OK or a negative status.
+ */
+int h3_qk_norm_rope(void* q, int64_t q_row_stride, void* k, int64_t k_row_stride,
+                    const void* wq, const void* wk, const int32_t* pos_thw,
+                    int64_t n_rows, int n_heads, int head_dim,
+                    int rot_t, int rot_h, int rot_w, float theta, float eps,
+                    h3_stream_t stream);
+
+/*
+ * h3_attention -- non-causal softmax(Q K^T * scale) V over packed sequences
+ * or grouped query ranges, in one launch.
+ *
+ * Follows the packed joint sequence with a valid length (vLLM-Omni blog,
+ * section 3.1: the attention backend receives the valid sequence length and
+ * the structural suffix padding costs nothing) and the grouped condition /
+ * audio / video query ranges over different KV extents of a contiguous
+ * history cache (SolarWM-H3 Realtime blog, stages 2 and 3).
+ *
+ * Segment b (0 <= b < n_seq) owns query rows [cu_seqlens_q[b], cu_seqlens_q[b+1])
+ * of q and out, and key/value rows [cu_seqlens_kv[b], cu_seqlens_kv[b+1]) of
+ * k and v.  If valid_len is non-NULL only the first valid_len[b] rows of both
+ * ranges are valid (self-attention over one padded buffer); otherwise every
+ * row of both ranges is.  For each valid query row i and head h:
+ *   out[i, h] = sum_j softmax_j(scale * <q[i, h], k[j, h]>) v[j, h]
+ * over the segment's valid key rows j.  Output rows past the valid length,
+ * and all rows of a segment with no valid key, are written as 0.  Padded
+ * input rows are never read, so they may hold anything (NaN, Inf).
+ *
+ * q, out      device bf16 [cu_seqlens_q[n_seq], n_heads, 128]
+ * k, v        device bf16 [cu_seqlens_kv[n_seq], n_heads, 128]
+ * cu_seqlens_q, cu_seqlens_kv
+ *             HOST int32 [n_seq + 1], start at 0, non-decreasing.
+ * valid_len   HOST int32 [n_seq] or NULL; 0 <= valid_len[b] <= both extents.
+ * n_seq       1 .. H3_MAX_SEGMENTS.
+ * scale       > 0 and finite (1/sqrt(128) for the DiT block).
+ * Alignment:  all four base pointers 16-byte aligned; row strides * 2 a
+ *             multiple of 16.  out must not overlap q, k or v.
+ * The host arrays are read during the call only, so the call can be
+ * captured in a CUDA graph.
+ * Returns H3_OK or a negative status.
+ */
+int h3_attention(const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,
+                 const void* v, int64_t v_row_stride, void* out, int64_t out_row_stride,
+                 const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                 const int32_t* valid_len, int n_seq, int n_heads, int head_dim,
+                 float scale, h3_stream_t stream);
+
+/* Message for the last nonzero status returned to the calling thread
+ * ("" if none).  The pointer stays valid until the thread's next call. */
+const char* h3_last_error(void);
+
+/*
+ * Debug: synchronise the current device, copy the device status word (an OR
+ * of H3_STATUS_* bits set by kernels whose bounded waits gave up) to *out and
+ * clear it.  Returns H3_OK, H3_ERR_ARG for a NULL out, or H3_ERR_DEVICE.
+ */
+int h3_status_word(uint32_t* out);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int h3_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* H3KERN_H */

@@ -1,0 +1,141 @@
+"""Packed-sequence attention for the MiniMax-H3 DiT block on GB300 (sm_103a).
+
+Two operations, both hand-written CUDA behind the C ABI of libh3kern.so
+(include/h3kern.h); this module only marshals torch tensors into pointers,
+strides and the current stream:
+
+* ``qk_norm_rope`` -- fused Q/K RMSNorm + axial 3-D RoPE, in place
+  (Sol-H3, arXiv 2609.35110, section 3.5 "Kernel Fusion", operator group 2).
+* ``attention`` -- softmax(Q K^T * scale) V over packed sequences with a
+  valid length, or over grouped query ranges with their own KV extents
+  (vLLM-Omni blog section 3.1; SolarWM-H3 Realtime blog stage 2).
+
+There is no CPU or library fallback: without the built library, or off an
+sm_103 device, every call raises ``H3Error``.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from typing import Optional, Sequence
+
+import torch
+
+from . import _binding
+
+__all__ = ["H3Error", "qk_norm_rope", "attention", "status_word", "lib", "HEAD_DIM",
+           "MAX_SEGMENTS", "attention_block"]
+
+HEAD_DIM = 128
+MAX_SEGMENTS = 16
+
+
+class H3Error(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_binding.STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+def lib():
+    return _binding.load()
+
+
+def _check(status: int):
+    if status != 0:
+        raise H3Error(status, lib().h3_last_error().decode())
+
+
+def _row_stride(t: torch.Tensor, name: str) -> int:
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if t.dim() != 3 or t.shape[-1] != HEAD_DIM:
+        raise ValueError(f"{name} must be [rows, heads, {HEAD_DIM}], got {tuple(t.shape)}")
+    if t.stride(-1) != 1 or (t.shape[1] > 1 and t.stride(1) != HEAD_DIM):
+        raise ValueError(f"{name}: channels must be contiguous and heads {HEAD_DIM} apart")
+    return t.stride(0) if t.shape[0] > 1 else t.shape[1] * HEAD_DIM
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def qk_norm_rope(q: torch.Tensor, k: torch.Tensor, wq: torch.Tensor, wk: torch.Tensor,
+                 pos_thw: torch.Tensor, n_rows: Optional[int] = None,
+                 rot=(32, 48, 48), theta: float = 10000.0, eps: float = 1e-6,
+                 stream=None) -> None:
+    """In place: q, k <- RoPE(RMSNorm(x) * w) for rows [0, n_rows)."""
+    qs, ks = _row_stride(q, "q"), _row_stride(k, "k")
+    H = q.shape[1]
+    if n_rows is None:
+        n_rows = q.shape[0]
+    if not (0 <= n_rows <= min(q.shape[0], k.shape[0], pos_thw.shape[0])):
+        raise ValueError("n_rows exceeds the tensors")
+    if pos_thw.dtype != torch.int32 or not pos_thw.is_contiguous() or pos_thw.shape[-1] != 3:
+        raise ValueError("pos_thw must be contiguous int32 [rows, 3]")
+    for w, name in ((wq, "wq"), (wk, "wk")):
+        if w.dtype != torch.bfloat16 or not w.is_contiguous() or tuple(w.shape) != (H, HEAD_DIM):
+            raise ValueError(f"{name} must be contiguous bf16 [{H}, {HEAD_DIM}]")
+    _check(lib().h3_qk_norm_rope(q.data_ptr(), qs, k.data_ptr(), ks, wq.data_ptr(),
+                                 wk.data_ptr(), pos_thw.data_ptr(), int(n_rows), H, HEAD_DIM,
+                                 int(rot[0]), int(rot[1]), int(rot[2]), float(theta),
+                                 float(eps), _stream(stream)))
+
+
+def _i32_array(values: Sequence[int]):
+    arr = (ctypes.c_int32 * len(values))(*[int(v) for v in values])
+    return arr
+
+
+def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+              cu_seqlens_q: Sequence[int], cu_seqlens_kv: Sequence[int],
+              valid_len: Optional[Sequence[int]] = None, scale: Optional[float] = None,
+              out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """out[i, h] = softmax_j(scale <q_i, k_j>) v_j per segment; see h3kern.h.
+
+    ``cu_seqlens_*`` and ``valid_len`` are host sequences of ints."""
+    H = q.shape[1]
+    if out is None:
+        out = torch.empty((q.shape[0], H, HEAD_DIM), dtype=torch.bfloat16, device=q.device)
+    strides = [_row_stride(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"))]
+    n_seq = len(cu_seqlens_q) - 1
+    if len(cu_seqlens_kv) != n_seq + 1 or (valid_len is not None and len(valid_len) != n_seq):
+        raise ValueError("cu_seqlens_q, cu_seqlens_kv and valid_len disagree on n_seq")
+    if cu_seqlens_q[-1] > q.shape[0] or cu_seqlens_q[-1] > out.shape[0] or \
+            cu_seqlens_kv[-1] > k.shape[0] or cu_seqlens_kv[-1] > v.shape[0]:
+        raise ValueError("cu_seqlens exceed the tensors")
+    if scale is None:
+        scale = 1.0 / math.sqrt(HEAD_DIM)
+    cq, ckv = _i32_array(cu_seqlens_q), _i32_array(cu_seqlens_kv)
+    vl = _i32_array(valid_len) if valid_len is not None else None
+    _check(lib().h3_attention(q.data_ptr(), strides[0], k.data_ptr(), strides[1],
+                              v.data_ptr(), strides[2], out.data_ptr(), strides[3],
+                              ctypes.cast(cq, _binding.c_i32p), ctypes.cast(ckv, _binding.c_i32p),
+                              ctypes.cast(vl, _binding.c_i32p) if vl is not None else None,
+                              n_seq, H, HEAD_DIM, float(scale), _stream(stream)))
+    return out
+
+
+def attention_block(q, k, v, wq, wk, pos_thw, cu_seqlens, valid_len,
+                    rot=(32, 48, 48), theta=10000.0, eps=1e-6, scale=None, out=None,
+                    stream=None) -> torch.Tensor:
+    """The block's hot path: fused Q/K norm + RoPE on the valid rows of each
+    packed sequence, then attention over the valid rows.  Q and K are
+    modified in place."""
+    for b in range(len(cu_seqlens) - 1):
+        r0 = cu_seqlens[b]
+        n = valid_len[b] if valid_len is not None else cu_seqlens[b + 1] - r0
+        if n:
+            qk_norm_rope(q[r0:], k[r0:], wq, wk, pos_thw[r0:], n_rows=n, rot=rot,
+                         theta=theta, eps=eps, stream=stream)
+    return attention(q, k, v, cu_seqlens, cu_seqlens, valid_len, scale, out, stream)
+
+
+def status_word() -> int:
+    """Synchronise the device; return and clear the device status bits."""
+    val = ctypes.c_uint32(0)
+    _check(lib().h3_status_word(ctypes.byref(val)))
+    return val.value

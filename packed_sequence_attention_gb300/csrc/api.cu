@@ -1,0 +1,188 @@
+// C-ABI front end of libh3kern: argument checks on the host, device checks,
+// then one launch per call.  See include/h3kern.h for the contract.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "h3_internal.h"
+#include "h3kern_debug.h"
+
+namespace h3 {
+void set_fault_next(int f);
+}
+
+namespace {
+
+thread_local std::string t_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return code;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Current device must be compute capability 10.3 (the kernels are built for
+// sm_103a only).  The answer is cached per device.
+int check_device() {
+  static std::atomic<int> cache[64];  // 0 unknown, 1 sm_103, 2 other
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(H3_ERR_DEVICE, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev >= 0 && dev < 64) {
+    const int c = cache[dev].load();
+    if (c == 1) return H3_OK;
+    if (c == 2) return fail(H3_ERR_ARCH, "device %d is not sm_103", dev);
+  }
+  int major = 0, minor = 0;
+  e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (e != cudaSuccess)
+    return fail(H3_ERR_DEVICE, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+  const bool ok = (major == 10 && minor == 3);
+  if (dev >= 0 && dev < 64) cache[dev].store(ok ? 1 : 2);
+  if (!ok) return fail(H3_ERR_ARCH, "device %d is sm_%d%d, the kernels need sm_103", dev, major, minor);
+  return H3_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int h3_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+const char* h3_last_error(void) { return t_last_error.c_str(); }
+
+int h3_qk_norm_rope(void* q, int64_t q_row_stride, void* k, int64_t k_row_stride, const void* wq,
+                    const void* wk, const int32_t* pos_thw, int64_t n_rows, int n_heads,
+                    int head_dim, int rot_t, int rot_h, int rot_w, float theta, float eps,
+                    h3_stream_t stream) {
+  if (n_rows < 0) return fail(H3_ERR_ARG, "n_rows must be >= 0 (got %lld)", (long long)n_rows);
+  if (n_heads < 1) return fail(H3_ERR_ARG, "n_heads must be >= 1 (got %d)", n_heads);
+  if (head_dim != h3::kHeadDim) return fail(H3_ERR_SHAPE, "head_dim must be 128 (got %d)", head_dim);
+  if (rot_t < 0 || rot_h < 0 || rot_w < 0 || (rot_t | rot_h | rot_w) & 1)
+    return fail(H3_ERR_SHAPE, "rotary sections must be even and >= 0 (got %d/%d/%d)", rot_t, rot_h,
+                rot_w);
+  if (rot_t + rot_h + rot_w > head_dim)
+    return fail(H3_ERR_SHAPE, "rotary sections sum to %d > head_dim %d", rot_t + rot_h + rot_w,
+                head_dim);
+  if (!std::isfinite(theta) || !(theta > 0.0f))
+    return fail(H3_ERR_ARG, "theta must be finite and > 0");
+  if (!std::isfinite(eps) || eps < 0.0f) return fail(H3_ERR_ARG, "eps must be finite and >= 0");
+  const int64_t width = static_cast<int64_t>(n_heads) * h3::kHeadDim;
+  if (q_row_stride < width || k_row_stride < width)
+    return fail(H3_ERR_SHAPE, "row strides (%lld, %lld) must be >= n_heads*128 = %lld",
+                (long long)q_row_stride, (long long)k_row_stride, (long long)width);
+  if (n_rows == 0) return H3_OK;
+  if (!q || !k || !wq || !wk || !pos_thw) return fail(H3_ERR_ARG, "null pointer argument");
+  if (q == k) return fail(H3_ERR_ARG, "q and k must be distinct buffers");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(wq) || !aligned16(wk))
+    return fail(H3_ERR_ALIGN, "q, k, wq, wk must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(pos_thw) & 3u) != 0)
+    return fail(H3_ERR_ALIGN, "pos_thw must be 4-byte aligned");
+  if ((q_row_stride * 2) % 16 != 0 || (k_row_stride * 2) % 16 != 0)
+    return fail(H3_ERR_ALIGN, "row strides must be multiples of 8 elements (16 bytes)");
+  if (n_rows > (int64_t(1) << 31) * 8)
+    return fail(H3_ERR_SHAPE, "n_rows too large for one launch");
+  int st = check_device();
+  if (st != H3_OK) return st;
+  h3::NormRopeArgs a{};
+  a.q = static_cast<__nv_bfloat16*>(q);
+  a.k = static_cast<__nv_bfloat16*>(k);
+  a.q_stride = q_row_stride;
+  a.k_stride = k_row_stride;
+  a.wq = static_cast<const __nv_bfloat16*>(wq);
+  a.wk = static_cast<const __nv_bfloat16*>(wk);
+  a.pos = pos_thw;
+  a.n_rows = n_rows;
+  a.n_heads = n_heads;
+  a.rot[0] = rot_t;
+  a.rot[1] = rot_h;
+  a.rot[2] = rot_w;
+  a.theta = theta;
+  a.eps = eps;
+  cudaError_t e = h3::launch_qk_norm_rope(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(H3_ERR_LAUNCH, "qk_norm_rope launch: %s", cudaGetErrorString(e));
+  return H3_OK;
+}
+
+int h3_attention(const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,
+                 const void* v, int64_t v_row_stride, void* out, int64_t out_row_stride,
+                 const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                 const int32_t* valid_len, int n_seq, int n_heads, int head_dim, float scale,
+                 h3_stream_t stream) {
+  if (n_seq < 1 || n_seq > H3_MAX_SEGMENTS)
+    return fail(H3_ERR_ARG, "n_seq must be in [1, %d] (got %d)", H3_MAX_SEGMENTS, n_seq);
+  if (n_heads < 1) return fail(H3_ERR_ARG, "n_heads must be >= 1 (got %d)", n_heads);
+  if (head_dim != h3::kHeadDim) return fail(H3_ERR_SHAPE, "head_dim must be 128 (got %d)", head_dim);
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return fail(H3_ERR_ARG, "scale must be finite and > 0");
+  if (!cu_seqlens_q || !cu_seqlens_kv) return fail(H3_ERR_ARG, "null cu_seqlens");
+  if (cu_seqlens_q[0] != 0 || cu_seqlens_kv[0] != 0)
+    return fail(H3_ERR_ARG, "cu_seqlens must start at 0");
+  for (int b = 0; b < n_seq; ++b) {
+    if (cu_seqlens_q[b + 1] < cu_seqlens_q[b] || cu_seqlens_kv[b + 1] < cu_seqlens_kv[b])
+      return fail(H3_ERR_ARG, "cu_seqlens must be non-decreasing (segment %d)", b);
+    if (valid_len) {
+      const int32_t lim = std::min(cu_seqlens_q[b + 1] - cu_seqlens_q[b],
+                                   cu_seqlens_kv[b + 1] - cu_seqlens_kv[b]);
+      if (valid_len[b] < 0 || valid_len[b] > lim)
+        return fail(H3_ERR_ARG, "valid_len[%d] = %d outside [0, %d]", b, valid_len[b], lim);
+    }
+  }
+  const int64_t width = static_cast<int64_t>(n_heads) * h3::kHeadDim;
+  if (q_row_stride < width || k_row_stride < width || v_row_stride < width ||
+      out_row_stride < width)
+    return fail(H3_ERR_SHAPE, "row strides must be >= n_heads*128 = %lld", (long long)width);
+  if (!q || !k || !v || !out) return fail(H3_ERR_ARG, "null tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(H3_ERR_ALIGN, "q, k, v, out must be 16-byte aligned");
+  if ((q_row_stride * 2) % 16 || (k_row_stride * 2) % 16 || (v_row_stride * 2) % 16 ||
+      (out_row_stride * 2) % 16)
+    return fail(H3_ERR_ALIGN, "row strides must be multiples of 8 elements (16 bytes)");
+  if (q_row_stride * 2 >= (int64_t(1) << 40) || k_row_stride * 2 >= (int64_t(1) << 40) ||
+      v_row_stride * 2 >= (int64_t(1) << 40))
+    return fail(H3_ERR_SHAPE, "row stride too large for a tensor map");
+  int st = check_device();
+  if (st != H3_OK) return st;
+  h3::AttnArgs a{};
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k = static_cast<const __nv_bfloat16*>(k);
+  a.v = static_cast<const __nv_bfloat16*>(v);
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.q_stride = q_row_stride;
+  a.k_stride = k_row_stride;
+  a.v_stride = v_row_stride;
+  a.out_stride = out_row_stride;
+  a.cu_q = cu_seqlens_q;
+  a.cu_kv = cu_seqlens_kv;
+  a.valid = valid_len;
+  a.n_seq = n_seq;
+  a.n_heads = n_heads;
+  a.scale = scale;
+  std::string err;
+  st = h3::launch_attention(a, reinterpret_cast<cudaStream_t>(stream), err);
+  if (st != H3_OK) return fail(st, "%s", err.c_str());
+  return H3_OK;
+}
+
+int h3_status_word(uint32_t* out) {
+  if (!out) return fail(H3_ERR_ARG, "out must not be NULL");
+  cudaError_t e = h3::read_and_clear_status(out);
+  if (e != cudaSuccess) return fail(H3_ERR_DEVICE, "status read: %s", cudaGetErrorString(e));
+  return H3_OK;
+}
+
+int h3_debug_fault_next_attention(int fault) {
+  if (fault < 0 || fault > 1) return fail(H3_ERR_ARG, "unknown fault %d", fault);
+  h3::set_fault_next(fault);
+  return H3_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,613 @@
+// Packed-sequence attention, sm_103a: TMA + tcgen05/TMEM flash attention.
+//
+// Computes out = softmax(Q K^T * scale) V per segment (a packed sequence
+// with a valid length, vLLM-Omni blog "MiniMax H3 on vLLM-Omni" section 3.1,
+// or a query group over its own KV range, SolarWM-H3 Realtime blog stage 2)
+// and per head, exactly, with the online-softmax recurrence of the
+// FlashAttention line of work: running row max m, running sum l, and a
+// rescale of the partial output whenever m moves.
+//
+// One CTA = one (segment, head, pair of 128-row query tiles).  Roles:
+//   warps 0-3  softmax for query tile 0 (thread i owns row i = TMEM lane i)
+//   warps 4-7  softmax for query tile 1
+//   warp  8    TMA producer: Q tiles once, then K/V tiles into a 2-stage ring
+//   warp  9    TMEM owner and single-thread tcgen05.mma issuer
+// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512);
+// P_t (bf16 pairs) overwrites the first 64 columns of S_t and feeds the
+// P.V product straight from TMEM.  Per KV tile j the issuer runs, in order,
+//   PV0(j)  QK0(j+1)  PV1(j)  QK1(j+1)
+// so that the softmax of one tile overlaps the MMAs of the other.  All
+// tcgen05.mma ops of the CTA execute in issue order, and a commit tracks
+// every earlier op of the issuing thread: S_t(j+1) complete therefore also
+// means PV_t(j) complete, which is what lets softmax rescale O_t in place.
+//
+// Masking: per-segment tensor maps have the segment's VALID row count as
+// their outer extent, so TMA zero-fills rows past it and never reads
+// padded rows (which may hold NaN/Inf); score columns past the valid
+// length are set to -inf with a select; query tiles wholly past it are
+// never scheduled.  Output rows past the valid length are written as 0.
+//
+// Every wait is bounded (wall-clock limit from %globaltimer).  A wait that
+// gives up sets a bit in the device status word and an abort epoch; the
+// CTA then drains its own in-flight copies and MMAs, frees TMEM and exits,
+// and other CTAs of the same launch stop at their next wait.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <vector>
+
+#include "h3_internal.h"
+#include "ptx.cuh"
+
+namespace h3 {
+
+__device__ uint32_t g_status;       // OR of H3_STATUS_* bits
+__device__ uint32_t g_abort_epoch;  // epoch of the last launch that gave up
+
+namespace {
+
+using namespace ptx;
+
+constexpr int kBM = 128;  // query rows per tile (MMA M)
+constexpr int kBN = 128;  // key rows per tile (MMA N of Q.K^T, K of P.V)
+constexpr int kNS = 2;    // K/V ring stages
+constexpr int kThreads = 320;
+constexpr uint32_t kTileBytes = kBM * kHeadDim * 2;  // 32 KB
+constexpr uint32_t kHalfBytes = kTileBytes / 2;      // 64 channels x 128 rows
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOffQ + 2 * kTileBytes;
+constexpr uint32_t kOffV = kOffK + kNS * kTileBytes;
+constexpr uint32_t kOffBar = kOffV + kNS * kTileBytes;
+enum {
+  BAR_Q = 0,
+  BAR_KFULL = 1,
+  BAR_VFULL = BAR_KFULL + kNS,
+  BAR_KVEMPTY = BAR_VFULL + kNS,
+  BAR_SFULL = BAR_KVEMPTY + kNS,
+  BAR_PFULL = BAR_SFULL + 2,
+  BAR_OFINAL = BAR_PFULL + 2,
+  BAR_DRAIN = BAR_OFINAL + 2,
+  NUM_BARS = BAR_DRAIN + 1
+};
+constexpr uint32_t kOffTmemSlot = kOffBar + NUM_BARS * 8;
+constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
+constexpr uint32_t kSmemUsed = kOffAbort + 4;
+constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColO = 256;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only if max grows by > 2^8
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, false, false);      // K-major Q, K
+constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kHeadDim, false, true);  // V is MN-major
+
+struct Seg {
+  int32_t q_row0;   // first row of the segment in q / out
+  int32_t nq;       // valid query rows (> 0)
+  int32_t nkv;      // valid key rows (> 0)
+  int32_t n_pairs;  // ceil(nq / 256)
+  int32_t cta0;     // first CTA of the segment
+  int32_t pad_;
+};
+
+struct __align__(128) AttnParams {
+  CUtensorMap tm_q[H3_MAX_SEGMENTS];
+  CUtensorMap tm_k[H3_MAX_SEGMENTS];
+  CUtensorMap tm_v[H3_MAX_SEGMENTS];
+  Seg seg[H3_MAX_SEGMENTS];  // schedule order (longest KV first)
+  int32_t zero_row0[H3_MAX_SEGMENTS];
+  int32_t zero_rows[H3_MAX_SEGMENTS];
+  __nv_bfloat16* out;
+  int64_t out_stride;
+  int64_t zero_chunks;  // 16-byte chunks to clear: sum(zero_rows) * n_heads * 16
+  int32_t n_seg, n_zero, n_heads, n_compute_ctas;
+  float scale_log2;
+  uint32_t epoch;
+  int32_t fault;  // test hook: 1 = the producer never loads K/V tile 1
+};
+
+struct WaitCtx {
+  volatile uint32_t* abort_smem;
+  uint32_t epoch;
+};
+
+__device__ __noinline__ void give_up(const WaitCtx& w, uint32_t bit) {
+  *w.abort_smem = 1u;
+  atomicOr(&g_status, bit);
+  atomicExch(&g_abort_epoch, w.epoch);
+}
+
+__device__ __forceinline__ bool should_stop(const WaitCtx& w) {
+  return *w.abort_smem != 0u || *reinterpret_cast<volatile uint32_t*>(&g_abort_epoch) == w.epoch;
+}
+
+// Single-thread bounded wait.  False = gave up (or another role did).
+__device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, const WaitCtx& w, uint32_t bit) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0u) {
+      if (should_stop(w)) {
+        *w.abort_smem = 1u;
+        return false;
+      }
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        give_up(w, bit);
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait that only ends on completion or time (no early stop): used to
+// drain operations already in flight before the CTA exits.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+// Warp-wide bounded wait; the decision is uniform across the warp.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const WaitCtx& w, uint32_t bit) {
+  const int lane = threadIdx.x & 31;
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    const bool ok = mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    if ((it & 63u) == 63u) {
+      int stop = 0;
+      if (lane == 0) {
+        if (t0 == 0) t0 = globaltimer_ns();
+        if (should_stop(w)) {
+          stop = 1;
+        } else if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          give_up(w, bit);
+          stop = 1;
+        }
+      }
+      if (__shfl_sync(0xffffffffu, stop, 0)) {
+        *w.abort_smem = 1u;
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void zero_fill(const AttnParams& p) {
+  const int64_t n = p.zero_chunks;
+  const int64_t per_row = static_cast<int64_t>(p.n_heads) * 16;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * 256;
+  for (int64_t c = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; c < n; c += stride) {
+    int64_t rem = c;
+    int r = 0;
+    while (r + 1 < p.n_zero && rem >= static_cast<int64_t>(p.zero_rows[r]) * per_row) {
+      rem -= static_cast<int64_t>(p.zero_rows[r]) * per_row;
+      ++r;
+    }
+    const int64_t row = p.zero_row0[r] + rem / per_row;
+    const int64_t col = (rem % per_row) * 8;  // element offset within the row's H*128
+    *reinterpret_cast<uint4*>(p.out + row * p.out_stride + col) = make_uint4(0, 0, 0, 0);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (p.zero_chunks > 0 && threadIdx.x < 256) zero_fill(p);
+  if (static_cast<int>(blockIdx.x) >= p.n_compute_ctas) return;
+
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (sbase - raw);
+  auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + kOffAbort);
+  const WaitCtx wctx{abort_flag, p.epoch};
+
+  // ---- work item
+  int si = 0;
+  while (si + 1 < p.n_seg && static_cast<int>(blockIdx.x) >= p.seg[si + 1].cta0) ++si;
+  const Seg sg = p.seg[si];
+  const int local = static_cast<int>(blockIdx.x) - sg.cta0;
+  const int head = local / sg.n_pairs;
+  const int qrow0 = (local - head * sg.n_pairs) * (2 * kBM);  // segment-relative
+  const int n_tiles = (qrow0 + kBM < sg.nq) ? 2 : 1;
+  const int n_kv = (sg.nkv + kBN - 1) / kBN;
+
+  // ---- set-up: barriers (thread 0), TMEM (warp 9)
+  if (threadIdx.x == 0) {
+    mbar_init(bar(BAR_Q), 1);
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(bar(BAR_KFULL + s), 1);
+      mbar_init(bar(BAR_VFULL + s), 1);
+      mbar_init(bar(BAR_KVEMPTY + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(BAR_SFULL + t), 1);
+      mbar_init(bar(BAR_PFULL + t), 4);  // one arrive per softmax warp
+      mbar_init(bar(BAR_OFINAL + t), 1);
+    }
+    mbar_init(bar(BAR_DRAIN), 1);
+    fence_mbar_init();
+    *abort_flag =
+        (*reinterpret_cast<volatile uint32_t*>(&g_abort_epoch) == p.epoch) ? 1u : 0u;
+  }
+  if (warp == 9) {
+    tmem_alloc(sbase + kOffTmemSlot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + kOffTmemSlot);
+
+  if (warp == 8) {
+    // ================================================= TMA producer
+    if (lane == 0 && *abort_flag == 0u) {
+      const CUtensorMap* tq = &p.tm_q[si];
+      const CUtensorMap* tk = &p.tm_k[si];
+      const CUtensorMap* tv = &p.tm_v[si];
+      prefetch_tmap(tq);
+      prefetch_tmap(tk);
+      prefetch_tmap(tv);
+      mbar_arrive_expect_tx(bar(BAR_Q), n_tiles * kTileBytes);
+      for (int t = 0; t < n_tiles; ++t)
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(sbase + kOffQ + t * kTileBytes + h * kHalfBytes, tq, bar(BAR_Q), h * 64,
+                      head, qrow0 + t * kBM);
+      int armed[kNS];
+      for (int s = 0; s < kNS; ++s) armed[s] = -1;
+      bool ok = true;
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int s = j % kNS, use = j / kNS;
+        if (j >= kNS) ok = wait1(bar(BAR_KVEMPTY + s), (use - 1) & 1, wctx, H3_STATUS_TIMEOUT_LOAD);
+        if (!ok) break;
+        if (p.fault == 1 && j == 1) continue;  // test hook: leave this stage empty
+        mbar_arrive_expect_tx(bar(BAR_KFULL + s), kTileBytes);
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(sbase + kOffK + s * kTileBytes + h * kHalfBytes, tk, bar(BAR_KFULL + s),
+                      h * 64, head, j * kBN);
+        mbar_arrive_expect_tx(bar(BAR_VFULL + s), kTileBytes);
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(sbase + kOffV + s * kTileBytes + h * kHalfBytes, tv, bar(BAR_VFULL + s),
+                      h * 64, head, j * kBN);
+        armed[s] = use;
+      }
+      if (*abort_flag != 0u) {
+        // Let every copy this CTA started land before the CTA exits.
+        drain_wait(bar(BAR_Q), 0);
+        for (int s = 0; s < kNS; ++s)
+          if (armed[s] >= 0) {
+            drain_wait(bar(BAR_KFULL + s), armed[s] & 1);
+            drain_wait(bar(BAR_VFULL + s), armed[s] & 1);
+          }
+      }
+    }
+    __syncwarp();  // lanes 1-31 wait here for lane 0
+  } else if (warp == 9) {
+    // ================================================= MMA issuer
+    if (lane == 0 && *abort_flag == 0u) {
+      auto qk = [&](int t, int s) {
+        const uint32_t qa = sbase + kOffQ + t * kTileBytes;
+        const uint32_t kb = sbase + kOffK + s * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+          mma_ss(tmem + kColS + t * 128, sdesc_sw128(qa + off, 16, 1024),
+                 sdesc_sw128(kb + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto pv = [&](int t, int s, bool acc) {
+        const uint32_t vb = sbase + kOffV + s * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          mma_ts(tmem + kColO + t * 128, tmem + kColS + t * 128 + kk * 8,
+                 sdesc_sw128(vb + kk * 2048, kHalfBytes, 1024), kIdescPV,
+                 (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = wait1(bar(BAR_Q), 0, wctx, H3_STATUS_TIMEOUT_MMA) &&
+                wait1(bar(BAR_KFULL), 0, wctx, H3_STATUS_TIMEOUT_MMA);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < n_tiles; ++t) {
+          qk(t, 0);
+          mma_commit(bar(BAR_SFULL + t));
+        }
+      }
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int s = j % kNS, use = j / kNS;
+        const int s2 = (j + 1) % kNS, use2 = (j + 1) / kNS;
+        const bool next = j + 1 < n_kv;
+        ok = wait1(bar(BAR_VFULL + s), use & 1, wctx, H3_STATUS_TIMEOUT_MMA);
+        for (int t = 0; t < n_tiles && ok; ++t) {
+          ok = wait1(bar(BAR_PFULL + t), j & 1, wctx, H3_STATUS_TIMEOUT_MMA);
+          if (!ok) break;
+          tc_fence_after();
+          pv(t, s, j > 0);
+          if (t == n_tiles - 1) mma_commit(bar(BAR_KVEMPTY + s));
+          if (next) {
+            if (t == 0) {
+              ok = wait1(bar(BAR_KFULL + s2), use2 & 1, wctx, H3_STATUS_TIMEOUT_MMA);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            qk(t, s2);
+            mma_commit(bar(BAR_SFULL + t));
+          } else {
+            mma_commit(bar(BAR_OFINAL + t));
+          }
+        }
+      }
+      // Every MMA issued above completes before TMEM is released.
+      mma_commit(bar(BAR_DRAIN));
+      drain_wait(bar(BAR_DRAIN), 0);
+    }
+    __syncwarp();
+  } else {
+    // ================================================= softmax (warps 0-7)
+    const int t = warp >> 2;
+    if (t < n_tiles && *abort_flag == 0u) {
+      const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+      const uint32_t tS = tmem + lane_base + kColS + t * 128;
+      const uint32_t tO = tmem + lane_base + kColO + t * 128;
+      const float c = p.scale_log2;
+      const int kv_tail = sg.nkv - (n_kv - 1) * kBN;  // valid columns of the last tile
+      float m_used = -INFINITY;
+      float l = 0.0f;
+      bool ok = true;
+      for (int j = 0; j < n_kv; ++j) {
+        ok = wait_warp(bar(BAR_SFULL + t), j & 1, wctx, H3_STATUS_TIMEOUT_SOFTMAX);
+        if (!ok) break;
+        tc_fence_after();
+        float s[4][32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, s[q]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_wait_ld(s[q]);
+        if (j == n_kv - 1 && kv_tail < kBN) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) s[q][i] = (q * 32 + i < kv_tail) ? s[q][i] : -INFINITY;
+        }
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[0][i], s[0][i + 8]);
+#pragma unroll
+        for (int i = 16; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[0][i]);
+#pragma unroll
+        for (int q = 1; q < 4; ++q)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[q][i]);
+        const float m_tile =
+            fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * c;
+        // Lazy rescaling: the running max only moves when the tile max
+        // exceeds it by more than 2^8, so p <= 256 and O / l stay exact.
+        const bool need = m_tile > m_used + kRescaleThreshold;
+        const float alpha = need ? ex2(m_used - m_tile) : 1.0f;  // 0 on the first tile
+        l *= alpha;
+        if (need) m_used = m_tile;
+        float ls[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ls[i] = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = ex2(fmaf(s[q][2 * i], c, -m_used));
+            const float p1 = ex2(fmaf(s[q][2 * i + 1], c, -m_used));
+            ls[i & 7] += p0 + p1;
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(tS + q * 16, pk);  // P columns 16q..16q+15 = scores 32q..32q+31
+        }
+        l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          // O_t holds PV(0..j-1), complete because S_t(j) is (in-order MMAs).
+          const float f = alpha;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float o[32];
+            tmem_ld32(tO + q * 32, o);
+            tmem_wait_ld(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= f;
+            tmem_st32(tO + q * 32, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_PFULL + t));
+      }
+      if (ok) ok = wait_warp(bar(BAR_OFINAL + t), 0, wctx, H3_STATUS_TIMEOUT_SOFTMAX);
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = 1.0f / l;
+        const int row = qrow0 + t * kBM + (warp & 3) * 32 + lane;  // segment-relative
+        const bool valid_row = row < sg.nq;
+        uint4* dst = reinterpret_cast<uint4*>(
+            p.out + static_cast<int64_t>(sg.q_row0 + row) * p.out_stride + head * kHeadDim);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float o[32];
+          tmem_ld32(tO + q * 32, o);
+          tmem_wait_ld(o);
+          uint32_t u[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) u[i] = pack_bf16x2(o[2 * i] * inv_l, o[2 * i + 1] * inv_l);
+          if (valid_row) {
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              dst[q * 4 + v4] = make_uint4(u[4 * v4], u[4 * v4 + 1], u[4 * v4 + 2], u[4 * v4 + 3]);
+          }
+        }
+      }
+    }
+  }
+
+  // ---- teardown: all TMEM reads and MMAs are complete here
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encoder(std::string& err) {
+  static EncodeTiledFn fn = nullptr;
+  static std::atomic<int> state{0};
+  if (state.load() == 1) return fn;
+  void* ptr = nullptr;
+  cudaDriverEntryPointQueryResult q{};
+  cudaError_t e =
+      cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || ptr == nullptr) {
+    err = std::string("cuTensorMapEncodeTiled unavailable: ") + cudaGetErrorString(e);
+    return nullptr;
+  }
+  fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  state.store(1);
+  return fn;
+}
+
+// [rows, n_heads, 128] bf16 starting at `base`, boxes of 64 channels x 1 head x 128 rows.
+bool encode_rows(EncodeTiledFn enc, CUtensorMap* m, const void* base, int64_t row_stride,
+                 int n_heads, int rows, std::string& err) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(n_heads),
+                              static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2,
+                                 static_cast<cuuint64_t>(row_stride) * 2};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kBN)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    err = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(static_cast<int>(r));
+    return false;
+  }
+  return true;
+}
+
+std::atomic<uint32_t> g_epoch_counter{0};
+std::atomic<int> g_fault_next{0};
+
+}  // namespace
+
+int launch_attention(const AttnArgs& a, cudaStream_t stream, std::string& err) {
+  EncodeTiledFn enc = get_encoder(err);
+  if (!enc) return H3_ERR_DEVICE;
+  thread_local AttnParams P;  // ~6.7 KB of kernel parameters, rebuilt on every call
+  std::memset(&P, 0, sizeof(P));
+
+  struct Item {
+    int b, q0, nq, kv0, nkv;
+  };
+  std::vector<Item> items;
+  P.n_zero = 0;
+  P.zero_chunks = 0;
+  for (int b = 0; b < a.n_seq; ++b) {
+    const int q0 = a.cu_q[b], q_ext = a.cu_q[b + 1] - a.cu_q[b];
+    const int kv0 = a.cu_kv[b], kv_ext = a.cu_kv[b + 1] - a.cu_kv[b];
+    int nq = a.valid ? a.valid[b] : q_ext;
+    const int nkv = a.valid ? a.valid[b] : kv_ext;
+    if (nkv == 0) nq = 0;  // no key: every query row of the segment is 0
+    if (nq > 0) items.push_back({b, q0, nq, kv0, nkv});
+    if (q_ext > nq) {
+      P.zero_row0[P.n_zero] = q0 + nq;
+      P.zero_rows[P.n_zero] = q_ext - nq;
+      P.zero_chunks += static_cast<int64_t>(q_ext - nq) * a.n_heads * 16;
+      ++P.n_zero;
+    }
+  }
+  // Longest KV extent first, so that long work items start in the first wave.
+  std::stable_sort(items.begin(), items.end(),
+                   [](const Item& x, const Item& y) { return x.nkv > y.nkv; });
+  int64_t ctas = 0;
+  for (size_t i = 0; i < items.size(); ++i) {
+    const Item& it = items[i];
+    Seg& s = P.seg[i];
+    s.q_row0 = it.q0;
+    s.nq = it.nq;
+    s.nkv = it.nkv;
+    s.n_pairs = (it.nq + 2 * kBM - 1) / (2 * kBM);
+    s.cta0 = static_cast<int32_t>(ctas);
+    ctas += static_cast<int64_t>(s.n_pairs) * a.n_heads;
+    if (!encode_rows(enc, &P.tm_q[i], a.q + static_cast<int64_t>(it.q0) * a.q_stride, a.q_stride,
+                     a.n_heads, it.nq, err) ||
+        !encode_rows(enc, &P.tm_k[i], a.k + static_cast<int64_t>(it.kv0) * a.k_stride, a.k_stride,
+                     a.n_heads, it.nkv, err) ||
+        !encode_rows(enc, &P.tm_v[i], a.v + static_cast<int64_t>(it.kv0) * a.v_stride, a.v_stride,
+                     a.n_heads, it.nkv, err))
+      return H3_ERR_DEVICE;
+  }
+  if (ctas > 0x7fffffff) {
+    err = "too many work items for one launch";
+    return H3_ERR_SHAPE;
+  }
+  P.n_seg = static_cast<int32_t>(items.size());
+  P.n_heads = a.n_heads;
+  P.n_compute_ctas = static_cast<int32_t>(ctas);
+  P.out = a.out;
+  P.out_stride = a.out_stride;
+  P.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+  P.epoch = g_epoch_counter.fetch_add(1) + 1;
+  P.fault = g_fault_next.exchange(0);
+  int64_t grid = ctas;
+  if (grid == 0) {
+    if (P.zero_chunks == 0) return H3_OK;  // nothing to do
+    grid = std::min<int64_t>((P.zero_chunks + 255) / 256, 1024);
+  }
+
+  static std::atomic<int> attr_done[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && attr_done[dev].load() == 0) {
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) {
+      err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
+      return H3_ERR_DEVICE;
+    }
+    attr_done[dev].store(1);
+  }
+  attn_fwd_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(P);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    err = std::string("attention launch: ") + cudaGetErrorString(e);
+    return H3_ERR_LAUNCH;
+  }
+  return H3_OK;
+}
+
+cudaError_t read_and_clear_status(uint32_t* out) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyFromSymbol(out, g_status, sizeof(uint32_t));
+  if (e != cudaSuccess) return e;
+  const uint32_t zero = 0;
+  return cudaMemcpyToSymbol(g_status, &zero, sizeof(uint32_t));
+}
+
+// Test hook (not in the public header): the next h3_attention launch on any
+// thread runs with the given fault; 1 = the producer never loads K/V tile 1,
+// so the MMA issuer's bounded wait runs out.
+void set_fault_next(int f) { g_fault_next.store(f); }
+
+}  // namespace h3

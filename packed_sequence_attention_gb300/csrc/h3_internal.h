@@ -1,0 +1,52 @@
+// Internal interface between the C-ABI front end (api.cu) and the kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <string>
+
+#include "h3kern.h"
+
+namespace h3 {
+
+constexpr int kHeadDim = 128;
+
+// ---------------------------------------------------------------- prologue
+struct NormRopeArgs {
+  __nv_bfloat16* q;
+  __nv_bfloat16* k;
+  int64_t q_stride, k_stride;  // elements
+  const __nv_bfloat16* wq;
+  const __nv_bfloat16* wk;
+  const int32_t* pos;
+  int64_t n_rows;
+  int n_heads;
+  int rot[3];
+  float theta, eps;
+};
+// Validated arguments -> one launch on `stream`.
+cudaError_t launch_qk_norm_rope(const NormRopeArgs& a, cudaStream_t stream);
+
+// --------------------------------------------------------------- attention
+struct AttnArgs {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  __nv_bfloat16* out;
+  int64_t q_stride, k_stride, v_stride, out_stride;  // elements
+  const int32_t* cu_q;   // host [n_seq + 1]
+  const int32_t* cu_kv;  // host [n_seq + 1]
+  const int32_t* valid;  // host [n_seq] or nullptr
+  int n_seq, n_heads;
+  float scale;
+};
+// Validated arguments -> tensor maps, schedule, one launch.  Returns an
+// H3_* status and fills `err` on failure.
+int launch_attention(const AttnArgs& a, cudaStream_t stream, std::string& err);
+
+// Device status word: read (after a device synchronise) and clear.
+cudaError_t read_and_clear_status(uint32_t* out);
+
+}  // namespace h3

@@ -1,0 +1,123 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+symbol the public headers declare, and rejects bad arguments on the host
+before touching CUDA."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+import torch
+
+from packed_sequence_attention_gb300 import _binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+H3_OK, ARG, ALIGN, SHAPE, ARCH, LAUNCH, TIMEOUT, DEVICE = 0, -1, -2, -3, -4, -5, -6, -7
+A = 0x10000  # a 16-byte-aligned fake device address; never dereferenced on the host
+
+
+def declared_symbols():
+    names = set()
+    for path in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(path).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names.update(re.findall(r"\b(h3_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_headers_declare_the_boundary():
+    names = declared_symbols()
+    assert {"h3_qk_norm_rope", "h3_attention", "h3_last_error", "h3_status_word"} <= set(names)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert name in _binding.SIGNATURES, f"{name} has no binding"
+
+
+def test_version(lib):
+    assert lib.h3_version() == 10000
+
+
+def _i32(vals):
+    return ctypes.cast((ctypes.c_int32 * len(vals))(*vals), _binding.c_i32p)
+
+
+def norm_rope(lib, **kw):
+    a = dict(q=A, qs=5376, k=A + 0x100000, ks=5376, wq=A, wk=A, pos=A, n=10, H=42, D=128,
+             rt=32, rh=48, rw=48, theta=10000.0, eps=1e-6, stream=None)
+    a.update(kw)
+    return lib.h3_qk_norm_rope(a["q"], a["qs"], a["k"], a["ks"], a["wq"], a["wk"], a["pos"],
+                               a["n"], a["H"], a["D"], a["rt"], a["rh"], a["rw"], a["theta"],
+                               a["eps"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n=-1), ARG), (dict(H=0), ARG), (dict(D=64), SHAPE), (dict(rt=31), SHAPE),
+    (dict(rt=-2), SHAPE), (dict(rt=64, rh=64, rw=2), SHAPE), (dict(theta=0.0), ARG),
+    (dict(theta=float("inf")), ARG), (dict(eps=-1.0), ARG), (dict(eps=float("nan")), ARG),
+    (dict(qs=5375), SHAPE), (dict(ks=100), SHAPE), (dict(q=None), ARG), (dict(pos=None), ARG),
+    (dict(k=A), ARG), (dict(q=A + 8), ALIGN), (dict(wk=A + 4), ALIGN), (dict(pos=A + 2), ALIGN),
+    (dict(qs=5380), ALIGN), (dict(ks=5377), ALIGN),
+])
+def test_norm_rope_rejects_on_host(lib, kw, code):
+    assert norm_rope(lib, **kw) == code
+    assert lib.h3_last_error().decode() != ""
+
+
+def test_norm_rope_zero_rows_is_a_no_op(lib):
+    assert norm_rope(lib, n=0, q=None, k=None) == H3_OK
+
+
+def attn(lib, **kw):
+    a = dict(q=A, qs=5376, k=A, ks=5376, v=A, vs=5376, o=A + 0x100000, os=5376,
+             cq=[0, 256], ckv=[0, 256], valid=[250], n_seq=None, H=42, D=128, scale=0.08838,
+             stream=None)
+    a.update(kw)
+    n_seq = a["n_seq"] if a["n_seq"] is not None else (len(a["cq"]) - 1 if a["cq"] else 1)
+    return lib.h3_attention(a["q"], a["qs"], a["k"], a["ks"], a["v"], a["vs"], a["o"], a["os"],
+                            _i32(a["cq"]) if a["cq"] is not None else None,
+                            _i32(a["ckv"]) if a["ckv"] is not None else None,
+                            _i32(a["valid"]) if a["valid"] is not None else None,
+                            n_seq, a["H"], a["D"], a["scale"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n_seq=0), ARG), (dict(n_seq=17, cq=[0] * 18, ckv=[0] * 18, valid=None), ARG),
+    (dict(H=0), ARG), (dict(D=256), SHAPE), (dict(scale=0.0), ARG), (dict(scale=-1.0), ARG),
+    (dict(scale=float("nan")), ARG), (dict(cq=None), ARG), (dict(cq=[1, 256]), ARG),
+    (dict(ckv=[0, 256, 100], cq=[0, 10, 20], valid=None), ARG),
+    (dict(valid=[257]), ARG), (dict(valid=[-1]), ARG),
+    (dict(cq=[0, 100], ckv=[0, 256], valid=[101]), ARG),
+    (dict(qs=100), SHAPE), (dict(os=5000), SHAPE), (dict(v=None), ARG), (dict(o=None), ARG),
+    (dict(q=A + 2), ALIGN), (dict(o=A + 8), ALIGN), (dict(ks=5377), ALIGN), (dict(os=5380), ALIGN),
+])
+def test_attention_rejects_on_host(lib, kw, code):
+    assert attn(lib, **kw) == code
+    assert lib.h3_last_error().decode() != ""
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+def test_valid_call_without_gpu_reports_device_error(lib):
+    assert attn(lib) == DEVICE
+    assert norm_rope(lib) == DEVICE
+    v = ctypes.c_uint32(0)
+    assert lib.h3_status_word(ctypes.byref(v)) == DEVICE
+
+
+def test_status_word_null(lib):
+    assert lib.h3_status_word(None) == ARG
+
+
+def test_fault_hook_validates(lib):
+    assert lib.h3_debug_fault_next_attention(7) == ARG
+    assert lib.h3_debug_fault_next_attention(0) == H3_OK
+
+
+def test_python_api_fails_loudly_without_library(monkeypatch, tmp_path):
+    import packed_sequence_attention_gb300 as h3
+    monkeypatch.setattr(_binding, "_LIB", None)
+    monkeypatch.setattr(_binding, "lib_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        h3.lib()
