@@ -60,7 +60,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
@@ -226,6 +226,15 @@ def bench_gpu(args):
     attn_tflops = flops / (attn_ms * 1e-3) / 1e12
     pro_gbs = w.prologue_bytes() / (pro_ms * 1e-3) / 1e9 if pro_ms > 0 else None
 
+    if args.kernels_only:
+        if rank == 0:
+            print(json.dumps({"workload": w.name, "attention_ms": attn_ms, "prologue_ms": pro_ms,
+                              "ms_per_step": ms_step, "attention_tflops": attn_tflops,
+                              "prologue_gbs": pro_gbs, "clocks": clk.summary()}))
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
     # ---- end to end through the public API, pinned host buffers
     host = {k: (v.cpu().pin_memory() if torch.is_tensor(v) else v) for k, v in
             W.make_inputs(w, device=f"cuda:{local}", seed=W.default_seed(w) + rank).items()}
@@ -376,15 +385,17 @@ def bench_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="h3", choices=["h3", "reference"])
     ap.add_argument("--config", default="full")
-    ap.add_argument("--cpu-heads", type=int, default=8)
-    ap.add_argument("--cpu-rows", type=int, default=64)
+    ap.add_argument("--cpu-heads", type=int, default=42)
+    ap.add_argument("--cpu-rows", type=int, default=192)
     ap.add_argument("--ref-heads", type=int, default=2)
     ap.add_argument("--ref-rows", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernels-only", action="store_true",
+                    help="profiling mode: warm-up and timed steps only (no e2e, no CPU baseline)")
     args = ap.parse_args()
     if args.impl == "reference":
         bench_reference(args)

@@ -131,9 +131,11 @@ int h3_attention(const void* q, int64_t q_row_stride, const void* k, int64_t k_r
 const char* h3_last_error(void);
 
 /*
- * Debug: synchronise the current device, copy the device status word (an OR
- * of H3_STATUS_* bits set by kernels whose bounded waits gave up) to *out and
- * clear it.  Returns H3_OK, H3_ERR_ARG for a NULL out, or H3_ERR_DEVICE.
+ * Synchronise the current device, copy the device status word (an OR of
+ * H3_STATUS_* bits set by kernels whose bounded waits gave up) to *out and
+ * clear it.  Returns H3_OK when no bit was set, H3_ERR_TIMEOUT when some
+ * were (the output of those launches is undefined), H3_ERR_ARG for a NULL
+ * out, or H3_ERR_DEVICE.
  */
 int h3_status_word(uint32_t* out);
 

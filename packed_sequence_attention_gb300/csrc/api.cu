@@ -176,6 +176,8 @@ int h3_status_word(uint32_t* out) {
   if (!out) return fail(H3_ERR_ARG, "out must not be NULL");
   cudaError_t e = h3::read_and_clear_status(out);
   if (e != cudaSuccess) return fail(H3_ERR_DEVICE, "status read: %s", cudaGetErrorString(e));
+  if (*out != 0u)
+    return fail(H3_ERR_TIMEOUT, "a bounded device wait gave up (status bits 0x%x)", *out);
   return H3_OK;
 }
 

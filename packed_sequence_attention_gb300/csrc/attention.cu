@@ -119,7 +119,12 @@ __device__ __noinline__ void give_up(const WaitCtx& w, uint32_t bit) {
 }
 
 __device__ __forceinline__ bool should_stop(const WaitCtx& w) {
-  return *w.abort_smem != 0u || *reinterpret_cast<volatile uint32_t*>(&g_abort_epoch) == w.epoch;
+  if (*w.abort_smem != 0u) return true;
+  if (*reinterpret_cast<volatile uint32_t*>(&g_abort_epoch) == w.epoch) {
+    atomicOr(&g_status, H3_STATUS_ABORTED);
+    return true;
+  }
+  return false;
 }
 
 // Single-thread bounded wait.  False = gave up (or another role did).

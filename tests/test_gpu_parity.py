@@ -287,11 +287,11 @@ def test_repeat_runs_bitwise_identical():
 
 @pytest.mark.parametrize("layout", ["packed_qkv", "row_pad"])
 def test_strided_views_match_contiguous_bitwise(layout):
-    base = to_dev(W.make_inputs("medium"))
+    base = W.make_inputs("medium", device="cuda")
     run_prologue(base)
     ref = run_attention(base).clone()
     kw = {"packed_qkv": True} if layout == "packed_qkv" else {"row_pad": 24}
-    g = to_dev(W.make_inputs("medium", **kw))
+    g = W.make_inputs("medium", device="cuda", **kw)
     assert g["q"].stride(0) != g["q"].shape[1] * 128
     run_prologue(g)
     out_buf = torch.full((4096, 42 * 128 + 64), float("nan"), dtype=torch.bfloat16, device="cuda")
