@@ -50,6 +50,7 @@ enum {
 #define H3_STATUS_TIMEOUT_MMA 0x2u    /* MMA issuer gave up waiting for data or P */
 #define H3_STATUS_TIMEOUT_SOFTMAX 0x4u/* softmax warps gave up waiting for S or O */
 #define H3_STATUS_ABORTED 0x8u        /* a CTA stopped early because another gave up */
+#define H3_STATUS_TIMEOUT_PROLOGUE 0x10u /* the Q/K prologue gave up waiting for a row */
 
 /*
  * h3_qk_norm_rope -- fused Q/K RMSNorm + axial 3-D RoPE, in place, one pass.
@@ -75,6 +76,7 @@ enum {
  * pos_thw     device int32 [n_rows, 3]: (t, h, w) position of each row.
  * n_rows      rows to process (0 = nothing to do); typically the valid rows.
  * head_dim    must be 128.
+ * n_heads     1 .. 448 (two staged rows must fit in shared memory).
  * rot_t/h/w   even, >= 0, rot_t + rot_h + rot_w <= 128 (the configs use 32/48/48).
  * theta       RoPE base (> 0, finite); eps >= 0, finite.
  * Alignment:  q, k, wq, wk 16-byte aligned; row strides * 2 bytes a multiple of 16;

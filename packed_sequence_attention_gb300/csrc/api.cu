@@ -67,6 +67,9 @@ int h3_qk_norm_rope(void* q, int64_t q_row_stride, void* k, int64_t k_row_stride
   if (n_rows < 0) return fail(H3_ERR_ARG, "n_rows must be >= 0 (got %lld)", (long long)n_rows);
   if (n_heads < 1) return fail(H3_ERR_ARG, "n_heads must be >= 1 (got %d)", n_heads);
   if (head_dim != h3::kHeadDim) return fail(H3_ERR_SHAPE, "head_dim must be 128 (got %d)", head_dim);
+  if (n_heads > h3::prologue_max_heads())
+    return fail(H3_ERR_SHAPE, "n_heads must be <= %d for the prologue (got %d)",
+                h3::prologue_max_heads(), n_heads);
   if (rot_t < 0 || rot_h < 0 || rot_w < 0 || (rot_t | rot_h | rot_w) & 1)
     return fail(H3_ERR_SHAPE, "rotary sections must be even and >= 0 (got %d/%d/%d)", rot_t, rot_h,
                 rot_w);

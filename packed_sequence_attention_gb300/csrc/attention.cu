@@ -296,23 +296,26 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   } else if (warp == 9) {
     // ================================================= MMA issuer
     if (lane == 0 && *abort_flag == 0u) {
+      // Descriptors are built once; a K step only moves the start address,
+      // which is the low field of the descriptor (addresses stay < 256 KB).
+      const uint64_t dq0 = sdesc_sw128(sbase + kOffQ, 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(sbase + kOffK, 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(sbase + kOffV, kHalfBytes, 1024);
       auto qk = [&](int t, int s) {
-        const uint32_t qa = sbase + kOffQ + t * kTileBytes;
-        const uint32_t kb = sbase + kOffK + s * kTileBytes;
+        const uint64_t qa = dq0 + ((t * kTileBytes) >> 4);
+        const uint64_t kb = dk0 + ((s * kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          mma_ss(tmem + kColS + t * 128, sdesc_sw128(qa + off, 16, 1024),
-                 sdesc_sw128(kb + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + kColS + t * 128, qa + off, kb + off, kIdescQK, kk > 0 ? 1u : 0u);
         }
       };
       auto pv = [&](int t, int s, bool acc) {
-        const uint32_t vb = sbase + kOffV + s * kTileBytes;
+        const uint64_t vb = dv0 + ((s * kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
-          mma_ts(tmem + kColO + t * 128, tmem + kColS + t * 128 + kk * 8,
-                 sdesc_sw128(vb + kk * 2048, kHalfBytes, 1024), kIdescPV,
-                 (acc || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + kColO + t * 128, tmem + kColS + t * 128 + kk * 8, vb + ((kk * 2048) >> 4),
+                 kIdescPV, (acc || kk > 0) ? 1u : 0u);
         }
       };
       bool ok = wait1(bar(BAR_Q), 0, wctx, H3_STATUS_TIMEOUT_MMA) &&
@@ -380,40 +383,47 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 #pragma unroll
             for (int i = 0; i < 32; ++i) s[q][i] = (q * 32 + i < kv_tail) ? s[q][i] : -INFINITY;
         }
+        // Row max: 8 independent chains of three-input max.
         float mx[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[0][i], s[0][i + 8]);
+        for (int i = 0; i < 8; ++i) mx[i] = fmax3(s[0][i], s[0][i + 8], s[0][i + 16]);
 #pragma unroll
-        for (int i = 16; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[0][i]);
+        for (int i = 24; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[0][i]);
 #pragma unroll
         for (int q = 1; q < 4; ++q)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[q][i]);
+          for (int i = 0; i < 16; ++i) mx[i & 7] = fmax3(mx[i & 7], s[q][i], s[q][i + 16]);
         const float m_tile =
-            fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * c;
+            fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * c;
         // Lazy rescaling: the running max only moves when the tile max
         // exceeds it by more than 2^8, so p <= 256 and O / l stay exact.
         const bool need = m_tile > m_used + kRescaleThreshold;
         const float alpha = need ? ex2(m_used - m_tile) : 1.0f;  // 0 on the first tile
         l *= alpha;
         if (need) m_used = m_tile;
+        // p = 2^(s*c - m) for pairs: packed FMA, two ex2, packed running sums.
         float ls[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) ls[i] = 0.0f;
+        const float neg_m = -m_used;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float p0 = ex2(fmaf(s[q][2 * i], c, -m_used));
-            const float p1 = ex2(fmaf(s[q][2 * i + 1], c, -m_used));
-            ls[i & 7] += p0 + p1;
+            float a0, a1;
+            ffma2(a0, a1, s[q][2 * i], s[q][2 * i + 1], c, c, neg_m, neg_m);
+            const float p0 = ex2(a0);
+            const float p1 = ex2(a1);
+            fadd2(ls[2 * (i & 3)], ls[2 * (i & 3) + 1], ls[2 * (i & 3)], ls[2 * (i & 3) + 1], p0, p1);
             pk[i] = pack_bf16x2(p0, p1);
           }
           tmem_st16(tS + q * 16, pk);  // P columns 16q..16q+15 = scores 32q..32q+31
         }
-        l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+        fadd2(ls[0], ls[1], ls[0], ls[1], ls[2], ls[3]);
+        fadd2(ls[4], ls[5], ls[4], ls[5], ls[6], ls[7]);
+        fadd2(ls[0], ls[1], ls[0], ls[1], ls[4], ls[5]);
+        l += ls[0] + ls[1];
         if (j > 0 && __any_sync(0xffffffffu, need)) {
           // O_t holds PV(0..j-1), complete because S_t(j) is (in-order MMAs).
           const float f = alpha;
@@ -423,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             tmem_ld32(tO + q * 32, o);
             tmem_wait_ld(o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= f;
+            for (int i = 0; i < 32; i += 2) fmul2(o[i], o[i + 1], o[i], o[i + 1], f, f);
             tmem_st32(tO + q * 32, o);
           }
         }
@@ -447,7 +457,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           tmem_wait_ld(o);
           uint32_t u[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) u[i] = pack_bf16x2(o[2 * i] * inv_l, o[2 * i + 1] * inv_l);
+          for (int i = 0; i < 16; ++i) {
+            fmul2(o[2 * i], o[2 * i + 1], o[2 * i], o[2 * i + 1], inv_l, inv_l);
+            u[i] = pack_bf16x2(o[2 * i], o[2 * i + 1]);
+          }
           if (valid_row) {
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4)
@@ -599,6 +612,20 @@ int launch_attention(const AttnArgs& a, cudaStream_t stream, std::string& err) {
     return H3_ERR_LAUNCH;
   }
   return H3_OK;
+}
+
+// Device address of the status word on the current device (looked up once
+// per device, with that device current), for kernels in other files.
+uint32_t* status_word_device_ptr() {
+  static uint32_t* ptrs[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<uint32_t*>(p);
+  }
+  return ptrs[dev];
 }
 
 cudaError_t read_and_clear_status(uint32_t* out) {

@@ -28,6 +28,10 @@ struct NormRopeArgs {
 };
 // Validated arguments -> one launch on `stream`.
 cudaError_t launch_qk_norm_rope(const NormRopeArgs& a, cudaStream_t stream);
+// Largest n_heads the prologue's shared-memory ring holds.
+int prologue_max_heads();
+// Device address of the status word on the current device (nullptr on error).
+uint32_t* status_word_device_ptr();
 
 // --------------------------------------------------------------- attention
 struct AttnArgs {

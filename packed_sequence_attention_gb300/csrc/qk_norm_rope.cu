@@ -4,32 +4,49 @@
 // (arXiv 2609.35110), section 3.5 "Kernel Fusion"; the vLLM-Omni blog
 // ("MiniMax H3 on vLLM-Omni"), section 3.2, fuses the same Q/K RMSNorm and
 // RoPE.  The point of the fusion is to read each wide activation once and
-// write it once.
+// write it once, so the kernel is built around keeping HBM busy:
 //
-// Work split: one warp per row r, covering both tensors and every head.
-// Lane l owns channel chunks [8s, 8s+8) and [64+8s, 64+8s+8) with s = l % 8,
-// and head-units u = l/8, l/8 + 4, ... of the 2*H units (q heads, then k
-// heads) of the row.  Each warp-wide 16-byte load therefore covers four
-// whole 128-byte segments, the 8 lanes of a head reduce the sum of squares
-// with three xor-shuffles, and the 8 (cos, sin) pairs a lane needs are
-// computed once per row and reused across all 2*H units.  Loads are issued
-// for kBatch units before any arithmetic so that each lane keeps
-// kBatch * 32 bytes in flight.
+// * Persistent CTAs of 128 threads walk items g = blockIdx.x + i * gridDim.x;
+//   item g is row g / 2 of Q (g even) or of K (g odd): n_heads * 256
+//   contiguous bytes.
+// * Thread 0 streams items into a 2-stage shared-memory ring with 1-D bulk
+//   async copies (cp.async.bulk, completion on an mbarrier): one item is in
+//   flight while the other is processed.  Small CTAs with a shallow ring let
+//   ~10 CTAs share an SM; on GB300 that beat deeper rings with fewer CTAs
+//   (58,758-row workload: 418 us vs 422 us for whole-row items with 128
+//   threads, 440 us with 256 threads, 444-569 us with 3-4 stages).
+// * Per item, threads 0..63 compute the (cos, sin) of the 64 channel pairs
+//   once into a per-stage table when the item's copy is issued (its position
+//   is fetched one ring-depth ahead); every head of the item reuses them.
+// * A head-vector (128 channels) is handled by 8 lanes, each owning channel
+//   chunks [8s, 8s+8) and [64+8s, 64+8s+8); the sum of squares is reduced with
+//   three xor-shuffles; results are rounded once to bf16 (RNE) and stored
+//   straight to global memory with 16-byte streaming stores.
+// * Every mbarrier wait is bounded; a wait that gives up sets a bit in the
+//   device status word and the CTA stops.
+#include <cmath>
+
 #include "h3_internal.h"
+#include "ptx.cuh"
 
 namespace h3 {
 namespace {
 
-constexpr int kWarpsPerBlock = 8;
-constexpr int kBatch = 7;  // units per lane in flight (7 * 32 B)
+using namespace ptx;
+
+constexpr int kThreads = 128;
+constexpr int kMaxStages = 4;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 struct NormRopeParams {
   __nv_bfloat16* x[2];
   int64_t stride[2];
   const __nv_bfloat16* w[2];
   const int32_t* pos;
+  uint32_t* status;
   int64_t n_rows;
   int n_heads;
+  int n_stages;
   float eps;
   float inv_freq[64];  // per channel pair p = (2p, 2p+1): theta^(-2j/d) of its section
   int32_t axis[64];    // 0 = t, 1 = h, 2 = w, -1 = not rotated
@@ -44,60 +61,126 @@ __device__ __forceinline__ void unpack8(const uint4 v, float* f) {
   }
 }
 
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // round to nearest even
-  return *reinterpret_cast<uint32_t*>(&h);
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
 }
 
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
-    qk_norm_rope_kernel(const __grid_constant__ NormRopeParams p) {
-  const int lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
-  if (row >= p.n_rows) return;
-  const int sub = lane & 7;
-  const int grp = lane >> 3;
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
 
-  // Rotation of this lane's 8 channel pairs for this row.
-  const int32_t* pr = p.pos + row * 3;
-  const float pos3[3] = {static_cast<float>(__ldg(pr)), static_cast<float>(__ldg(pr + 1)),
-                         static_cast<float>(__ldg(pr + 2))};
-  float cs[8], sn[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int pair = (i < 4) ? 4 * sub + i : 32 + 4 * sub + (i - 4);
-    const int ax = p.axis[pair];
-    if (ax < 0) {
-      cs[i] = 1.0f;
-      sn[i] = 0.0f;
-    } else {
-      sincosf(pos3[ax] * p.inv_freq[pair], &sn[i], &cs[i]);
+__global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_constant__ NormRopeParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int sub = lane & 7;                       // channel chunk of this lane
+  const int slot = (tid >> 5) * 4 + (lane >> 3);  // which head-unit of a pass
+  constexpr int kSlots = kThreads / 8;
+  const int H = p.n_heads;
+  const uint32_t row_bytes = static_cast<uint32_t>(H) * kHeadDim * 2;
+  const uint32_t stage_bytes = row_bytes;  // one tensor row per item
+  const int NST = p.n_stages;
+  const uint32_t sbase = smem_u32(smem);
+  float2* tab = reinterpret_cast<float2*>(smem + NST * stage_bytes);  // [NST][64] (cos, sin)
+  const uint32_t s_bar = sbase + NST * stage_bytes + NST * 64 * 8;   // mbarriers [NST]
+
+  const int64_t first = blockIdx.x;
+  const int64_t step = gridDim.x;
+  const int64_t n_items = 2 * p.n_rows;  // item g: row g >> 1, tensor g & 1
+  const int64_t n_mine = first < n_items ? (n_items - 1 - first) / step + 1 : 0;
+  const int my_axis = tid < 64 ? p.axis[tid] : -1;
+  const float my_freq = tid < 64 ? p.inv_freq[tid] : 0.0f;
+
+  // Position of row i of this CTA along this thread's pair axis (threads < 64).
+  auto load_pos = [&](int64_t i) -> int32_t {
+    if (my_axis < 0 || i >= n_mine) return 0;
+    return __ldg(p.pos + ((first + i * step) >> 1) * 3 + my_axis);
+  };
+  auto fill_table = [&](int s, int32_t pos) {
+    if (tid < 64) {
+      float c = 1.0f, sn = 0.0f;
+      if (my_axis >= 0) sincosf(static_cast<float>(pos) * my_freq, &sn, &c);
+      tab[s * 64 + tid] = make_float2(c, sn);
     }
-  }
+  };
+  auto issue = [&](int64_t i) {  // bytes of row i of this CTA -> stage i % NST
+    const int s = static_cast<int>(i % NST);
+    const int64_t g = first + i * step;
+    const int64_t row = g >> 1;
+    const int tt = static_cast<int>(g & 1);
+    const uint32_t bar = s_bar + 8 * s;
+    mbar_arrive_expect_tx(bar, stage_bytes);
+    bulk_load(sbase + s * stage_bytes, p.x[tt] + row * p.stride[tt], row_bytes, bar);
+  };
 
-  const int n_units = 2 * p.n_heads;
-  for (int base = 0; base < n_units; base += 4 * kBatch) {
-    uint4 xa[kBatch], xb[kBatch];
-#pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
-      const int u = base + 4 * b + grp;
-      if (u < n_units) {
-        const int t = u >= p.n_heads;
-        const int h = u - t * p.n_heads;
-        const uint4* src =
-            reinterpret_cast<const uint4*>(p.x[t] + row * p.stride[t] + h * kHeadDim);
-        xa[b] = __ldcs(src + sub);
-        xb[b] = __ldcs(src + 8 + sub);
-      } else {
-        xa[b] = make_uint4(0, 0, 0, 0);
-        xb[b] = make_uint4(0, 0, 0, 0);
+  if (tid == 0) {
+    for (int s = 0; s < NST; ++s) mbar_init(s_bar + 8 * s, 1);
+    fence_mbar_init();
+    for (int64_t i = 0; i < n_mine && i < NST; ++i) issue(i);
+  }
+  for (int64_t i = 0; i < n_mine && i < NST; ++i) fill_table(static_cast<int>(i), load_pos(i));
+  __syncthreads();
+
+  const int n_units = H;
+  for (int64_t i = 0; i < n_mine; ++i) {
+    const int s = static_cast<int>(i % NST);
+    const uint32_t parity = static_cast<uint32_t>((i / NST) & 1);
+    const int64_t row = (first + i * step) >> 1;
+    const int tsel = static_cast<int>((first + i * step) & 1);
+    const int32_t pos_ahead = load_pos(i + NST);  // in flight while this row is processed
+
+    // Wait for this row's bytes (bounded).
+    bool ok = mbar_try_wait(s_bar + 8 * s, parity);
+    if (!ok) {
+      const uint64_t t0 = globaltimer_ns();
+      while (!(ok = mbar_try_wait(s_bar + 8 * s, parity))) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) break;
       }
     }
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) {
+        atomicOr(p.status, H3_STATUS_TIMEOUT_PROLOGUE);
+        // Let the copies this CTA started land before it exits (bounded).
+        for (int64_t j = i; j < n_mine && j < i + NST; ++j) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(s_bar + 8 * (j % NST), static_cast<uint32_t>((j / NST) & 1)))
+            if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+        }
+      }
+      return;
+    }
+    float cs[8], sn[8];
 #pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
-      const int u = base + 4 * b + grp;
+    for (int j = 0; j < 8; ++j) {
+      const int pair = (j < 4) ? 4 * sub + j : 32 + 4 * sub + (j - 4);
+      const float2 v = tab[s * 64 + pair];
+      cs[j] = v.x;
+      sn[j] = v.y;
+    }
+    const uint32_t stage = sbase + s * stage_bytes;
+    for (int u0 = 0; u0 < n_units; u0 += kSlots) {
+      const int u = u0 + slot;
+      const bool live = u < n_units;
+      const int t = tsel;
+      const int h = live ? u : 0;
       float x[16];
-      unpack8(xa[b], x);
-      unpack8(xb[b], x + 8);
+      const uint32_t src = stage + h * (kHeadDim * 2) + sub * 16;
+      if (live) {
+        unpack8(lds128(src), x);
+        unpack8(lds128(src + 128), x + 8);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) x[c] = 0.0f;
+      }
       float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
       for (int c = 0; c < 16; c += 2) {
@@ -108,31 +191,38 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
       ss += __shfl_xor_sync(0xffffffffu, ss, 1);
       ss += __shfl_xor_sync(0xffffffffu, ss, 2);
       ss += __shfl_xor_sync(0xffffffffu, ss, 4);
-      if (u >= n_units) continue;  // uniform across the 8 lanes of a unit
+      if (!live) continue;  // uniform across the 8 lanes of a unit
       const float r = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
-      const int t = u >= p.n_heads;
-      const int h = u - t * p.n_heads;
       const uint4* wsrc = reinterpret_cast<const uint4*>(p.w[t] + h * kHeadDim);
       float w[16];
       unpack8(__ldg(wsrc + sub), w);
       unpack8(__ldg(wsrc + 8 + sub), w + 8);
       uint32_t o[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float y0 = x[2 * i] * r * w[2 * i];
-        const float y1 = x[2 * i + 1] * r * w[2 * i + 1];
-        const float z0 = y0 * cs[i] - y1 * sn[i];
-        const float z1 = y0 * sn[i] + y1 * cs[i];
-        o[i] = pack2(z0, z1);
+      for (int j = 0; j < 8; ++j) {
+        const float y0 = x[2 * j] * r * w[2 * j];
+        const float y1 = x[2 * j + 1] * r * w[2 * j + 1];
+        o[j] = pack_bf16x2(y0 * cs[j] - y1 * sn[j], y0 * sn[j] + y1 * cs[j]);
       }
       uint4* dst = reinterpret_cast<uint4*>(p.x[t] + row * p.stride[t] + h * kHeadDim);
       __stcs(dst + sub, make_uint4(o[0], o[1], o[2], o[3]));
       __stcs(dst + 8 + sub, make_uint4(o[4], o[5], o[6], o[7]));
     }
+    __syncthreads();  // stage s and table s are free again
+    if (i + NST < n_mine) {
+      if (tid == 0) issue(i + NST);
+      fill_table(s, pos_ahead);
+    }
   }
 }
 
 }  // namespace
+
+int prologue_max_heads() {
+  // Two stages of one tensor row (256 B per head) plus two cos/sin tables and
+  // the barriers must fit in 227 KB of shared memory: 452 heads; keep 448.
+  return 448;
+}
 
 cudaError_t launch_qk_norm_rope(const NormRopeArgs& a, cudaStream_t stream) {
   NormRopeParams p{};
@@ -146,6 +236,8 @@ cudaError_t launch_qk_norm_rope(const NormRopeArgs& a, cudaStream_t stream) {
   p.n_rows = a.n_rows;
   p.n_heads = a.n_heads;
   p.eps = a.eps;
+  p.status = status_word_device_ptr();
+  if (p.status == nullptr) return cudaErrorInvalidSymbol;
   // Per-pair section and inverse frequency, in double, rounded once.
   const int edges[3] = {a.rot[0], a.rot[0] + a.rot[1], a.rot[0] + a.rot[1] + a.rot[2]};
   for (int pair = 0; pair < 64; ++pair) {
@@ -167,8 +259,33 @@ cudaError_t launch_qk_norm_rope(const NormRopeArgs& a, cudaStream_t stream) {
       p.inv_freq[pair] = 0.0f;
     }
   }
-  const int64_t blocks = (a.n_rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  qk_norm_rope_kernel<<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(p);
+  // Ring depth: two stages (one item in flight while one is processed).
+  const size_t stage_bytes = 1ull * a.n_heads * kHeadDim * 2;
+  const int nst = 2;
+  p.n_stages = nst;
+  const size_t smem = nst * (stage_bytes + 64 * 8) + kMaxStages * 8;
+  static int attr_done[64];
+  static size_t attr_smem[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_done[dev] || attr_smem[dev] < smem) {
+    e = cudaFuncSetAttribute(qk_norm_rope_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = 1;
+    attr_smem[dev] = smem;
+  }
+  int per_sm = 0, sms = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, qk_norm_rope_kernel, kThreads, smem);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  int64_t grid = static_cast<int64_t>(sms) * per_sm;
+  if (grid > 2 * a.n_rows) grid = 2 * a.n_rows;
+  qk_norm_rope_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -55,6 +55,7 @@ def norm_rope(lib, **kw):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(n=-1), ARG), (dict(H=0), ARG), (dict(D=64), SHAPE), (dict(rt=31), SHAPE),
+    (dict(H=449, qs=449 * 128, ks=449 * 128), SHAPE),
     (dict(rt=-2), SHAPE), (dict(rt=64, rh=64, rw=2), SHAPE), (dict(theta=0.0), ARG),
     (dict(theta=float("inf")), ARG), (dict(eps=-1.0), ARG), (dict(eps=float("nan")), ARG),
     (dict(qs=5375), SHAPE), (dict(ks=100), SHAPE), (dict(q=None), ARG), (dict(pos=None), ARG),

@@ -113,6 +113,21 @@ def test_prologue_rotary_splits(rot):
         prologue_bound(got, ref)
 
 
+@pytest.mark.parametrize("H,rows", [(1, 1), (7, 5), (42, 33), (200, 9), (448, 3)])
+def test_prologue_head_counts(H, rows):
+    w = W.custom(f"h{H}", H, [W.Segment(rows, rows, None, None, rows, 0)])
+    inp = W.make_inputs(w, seed=H)
+    g = to_dev(inp)
+    h3.qk_norm_rope(g["q"], g["k"], g["wq"], g["wk"], g["pos_thw"], rot=ROT)
+    torch.cuda.synchronize()
+    pos = inp["pos_thw"].numpy()
+    for t, wn in (("q", "wq"), ("k", "wk")):
+        ref = O.qk_norm_rope(O.widen(inp[t]), O.widen(inp[wn]), pos)
+        got = O.widen(g[t])
+        gate(got, ref, f"H={H} {t}")
+        prologue_bound(got, ref)
+
+
 def test_prologue_full_size_sampled():
     inp = W.make_inputs("full", device="cuda")
     q0, k0 = inp["q"].cpu(), inp["k"].cpu()
