@@ -327,6 +327,25 @@ def test_key_permutation_equivariance():
     gate(O.widen(b[:4000]), O.widen(a[:4000]), "permuted keys")
 
 
+@pytest.mark.parametrize("boost", [1.5, 6.0, 40.0])
+def test_attention_row_max_jumps(boost):
+    # Keys past row 300 are scaled up, so the row max of later KV tiles jumps
+    # by up to ~2^(boost * 12) over the first tile's: the softmax's exact
+    # rescaling path (and, for small boosts, the no-rescale path) must agree
+    # with the oracle.
+    H, L = 2, 700
+    gen = torch.Generator().manual_seed(int(boost * 10))
+    q = torch.randn((L, H, 128), generator=gen)
+    k = torch.randn((L, H, 128), generator=gen)
+    k[300:] *= boost
+    v = torch.randn((L, H, 128), generator=gen)
+    q, k, v = (x.to(torch.bfloat16) for x in (q, k, v))
+    out = h3.attention(q.cuda(), k.cuda(), v.cuda(), [0, L], [0, L], None, SCALE)
+    torch.cuda.synchronize()
+    ref = O.attention(O.widen(q), O.widen(k), O.widen(v), [0, L], [0, L], None, SCALE)
+    gate(O.widen(out), ref, f"boost {boost}")
+
+
 def test_closed_forms_on_gpu():
     # all V rows equal -> out = that row; single valid key -> out = v_0
     H, L = 2, 300
