@@ -212,6 +212,21 @@ def bench_gpu(args):
         dist.barrier()
     ms_total = t_start.elapsed_time(t_end)
     attn_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
+    # The prologue alone (in the step it follows the previous attention,
+    # whose last output lines are still being written back from L2).
+    pro_alone_ms = None
+    if w.self_attention:
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(10):
+            for b, s in enumerate(w.segments):
+                if s.n_valid_q():
+                    r0 = g["cu_seqlens_q"][b]
+                    h3.qk_norm_rope(g["q"][r0:], g["k"][r0:], g["wq"], g["wk"],
+                                    g["pos_thw"][r0:], n_rows=s.n_valid_q(), rot=ROT)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        pro_alone_ms = a0.elapsed_time(a1) / 10
     pro_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs])) if w.self_attention else 0.0
     status = h3.status_word()
     if status:
@@ -314,6 +329,9 @@ def bench_gpu(args):
         "prologue_gbs": round(pro_gbs, 1) if pro_gbs else None,
         "prologue_frac_hbm_measured": round(pro_gbs / pk["hbm"], 4) if pro_gbs else None,
         "prologue_frac_8tbs": round(pro_gbs / 8000.0, 4) if pro_gbs else None,
+        "prologue_alone_us": round(pro_alone_ms * 1e3, 2) if pro_alone_ms else None,
+        "prologue_alone_gbs": round(w.prologue_bytes() / (pro_alone_ms * 1e-3) / 1e9, 1)
+        if pro_alone_ms else None,
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 3)},
         "gpu_launches": launches_per_step(w) * args.steps,
