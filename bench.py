@@ -228,6 +228,7 @@ def bench_gpu(args):
         torch.cuda.synchronize()
         pro_alone_ms = a0.elapsed_time(a1) / 10
     pro_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs])) if w.self_attention else 0.0
+    lora = lora_prologue_timing(h3, g, w, stream, pk) if w.self_attention else None
     status = h3.status_word()
     if status:
         raise SystemExit(f"device status word {status:#x} after the timed region")
@@ -332,6 +333,7 @@ def bench_gpu(args):
         "prologue_alone_us": round(pro_alone_ms * 1e3, 2) if pro_alone_ms else None,
         "prologue_alone_gbs": round(w.prologue_bytes() / (pro_alone_ms * 1e-3) / 1e9, 1)
         if pro_alone_ms else None,
+        "next_rows": {"lora_prologue": lora},
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 3)},
         "gpu_launches": launches_per_step(w) * args.steps,
@@ -343,6 +345,52 @@ def bench_gpu(args):
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def lora_prologue_timing(h3, g, w, stream, pk, iters=10):
+    """The LoRA-consumer prologue (base + delta rounded to bf16, then the
+    norm + RoPE) against the separate branches it replaces (a bf16 add kernel
+    writing the sum, then the plain prologue).  Bytes: base and delta read,
+    result written."""
+    gen = torch.Generator(device=g["q"].device).manual_seed(77)
+    dq = (0.05 * torch.randn(g["q"].shape, generator=gen, device=g["q"].device)).to(torch.bfloat16)
+    dk = (0.05 * torch.randn(g["k"].shape, generator=gen, device=g["k"].device)).to(torch.bfloat16)
+
+    def fused():
+        for b, s in enumerate(w.segments):
+            if s.n_valid_q():
+                r0, n = g["cu_seqlens_q"][b], s.n_valid_q()
+                h3.qk_norm_rope_lora(g["q"][r0:], dq[r0:], g["k"][r0:], dk[r0:], g["wq"], g["wk"],
+                                     g["pos_thw"][r0:], n_rows=n, rot=ROT)
+
+    def separate():
+        for b, s in enumerate(w.segments):
+            if s.n_valid_q():
+                r0, n = g["cu_seqlens_q"][b], s.n_valid_q()
+                g["q"][r0:r0 + n].add_(dq[r0:r0 + n])
+                g["k"][r0:r0 + n].add_(dk[r0:r0 + n])
+                h3.qk_norm_rope(g["q"][r0:], g["k"][r0:], g["wq"], g["wk"], g["pos_thw"][r0:],
+                                n_rows=n, rot=ROT)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(iters):
+            fn()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        return a0.elapsed_time(a1) / iters * 1e3
+
+    us = timed(fused)
+    sep = timed(separate)
+    nbytes = 1.5 * (w.prologue_bytes() - 2 * 2 * w.n_heads * 128) + 2 * 2 * w.n_heads * 128
+    del dq, dk
+    return {"us": round(us, 2), "gbs": round(nbytes / us / 1e3, 1),
+            "frac_hbm_measured": round(nbytes / us / 1e3 / pk["hbm"], 4),
+            "bytes": nbytes, "separate_branches_us": round(sep, 2),
+            "speedup_vs_separate": round(sep / us, 3)}
 
 
 def committed_traffic(w):

@@ -90,6 +90,33 @@ int h3_qk_norm_rope(void* q, int64_t q_row_stride, void* k, int64_t k_row_stride
                     h3_stream_t stream);
 
 /*
+ * h3_qk_norm_rope_lora -- the same fused prologue as a LoRA consumer.
+ *
+ * Follows "Precision-preserving LoRA fusion" (Sol-H3, section 3.5): the base
+ * projection and the LoRA branch output stay separate tensors, and the
+ * consumer rounds base + delta to bf16 (fp32 sum, round-to-nearest-even)
+ * before the QK normalisation and RoPE, exactly where separate branches
+ * would have stored the sum.  The result is therefore bit-identical to
+ * adding the branches into a bf16 tensor first and then calling
+ * h3_qk_norm_rope, without the wide sum's HBM write and re-read.
+ *
+ * q, k        device bf16 [n_rows, n_heads, 128]: the base branch on input,
+ *             the normalised + rotated result on output (in place).
+ * q_delta, k_delta
+ *             device bf16 [n_rows, n_heads, 128] LoRA branch outputs, read only;
+ *             their row strides are in elements.
+ * n_heads     1 .. 220 (two staged rows of base + delta must fit in shared memory).
+ * All other arguments, alignment rules and errors as h3_qk_norm_rope; the
+ * delta pointers and strides follow the same 16-byte rules.
+ */
+int h3_qk_norm_rope_lora(void* q, int64_t q_row_stride, const void* q_delta,
+                         int64_t q_delta_row_stride, void* k, int64_t k_row_stride,
+                         const void* k_delta, int64_t k_delta_row_stride, const void* wq,
+                         const void* wk, const int32_t* pos_thw, int64_t n_rows, int n_heads,
+                         int head_dim, int rot_t, int rot_h, int rot_w, float theta, float eps,
+                         h3_stream_t stream);
+
+/*
  * h3_attention -- non-causal softmax(Q K^T * scale) V over packed sequences
  * or grouped query ranges, in one launch.
  *

@@ -43,3 +43,20 @@ def attention_row(qrow, keys, values, scale):
     d = len(values[0])
     return [math.fsum(e[j] * values[j][c] for j in range(len(values))) / z
             for c in range(d)]
+
+
+def round_bf16(x):
+    """Nearest bfloat16 to a Python float (8 significant bits), ties to even."""
+    if x == 0.0 or math.isinf(x) or math.isnan(x):
+        return x
+    m, e = math.frexp(x)
+    e = max(e, -125)
+    q = math.ldexp(1.0, e - 8)
+    return round(x / q) * q  # Python's round() is round-half-to-even
+
+
+def norm_rope_lora_row(base, delta, w, pos, sections, theta, eps):
+    """One (row, head) of the LoRA-fused prologue: round base + delta to bf16
+    first, then the RMSNorm + axial RoPE of ``norm_rope_row``."""
+    x = [round_bf16(b + d) for b, d in zip(base, delta)]
+    return norm_rope_row(x, w, pos, sections, theta, eps)

@@ -97,6 +97,34 @@ def qk_norm_rope(x: np.ndarray, w: np.ndarray, pos: np.ndarray,
     return rope_axial(y, pos, sections, theta)
 
 
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to the nearest bfloat16 (8 significant bits,
+    8-bit exponent), ties to even, as float64.  Values beyond the largest
+    finite bf16 become +-inf; the subnormal range keeps a fixed quantum of
+    2^-133."""
+    x = np.asarray(x, dtype=np.float64)
+    out = np.array(x, copy=True)
+    finite = np.isfinite(x) & (x != 0)
+    m, e = np.frexp(x[finite])                 # x = m * 2^e, 0.5 <= |m| < 1
+    e = np.maximum(e, -125)                    # below 2^-126 the quantum stays 2^-133
+    q = np.ldexp(1.0, e - 8)                   # value of one unit in the last place
+    r = np.rint(x[finite] / q) * q             # rint rounds half to even
+    big = np.abs(r) >= np.ldexp(1.0, 128)      # past the largest finite bf16
+    r[big] = np.copysign(np.inf, r[big])
+    out[finite] = r
+    return out
+
+
+def qk_norm_rope_lora(base: np.ndarray, delta: np.ndarray, w: np.ndarray, pos: np.ndarray,
+                      sections=DEFAULT_SECTIONS, theta=DEFAULT_THETA,
+                      eps=DEFAULT_EPS) -> np.ndarray:
+    """LoRA consumer fusion (Sol-H3 section 3.5 "Precision-preserving LoRA
+    fusion"): the consumer rounds base + delta to bf16 before the Q/K
+    normalisation and RoPE, exactly where the separate branches would store
+    the sum; the rest is ``qk_norm_rope`` on that rounded sum."""
+    return qk_norm_rope(round_bf16(base + delta), w, pos, sections, theta, eps)
+
+
 # --------------------------------------------------------------- attention
 def softmax_rows(s: np.ndarray) -> np.ndarray:
     """Row-wise softmax of a float64 score block (max-subtracted)."""

@@ -6,6 +6,8 @@ strides and the current stream:
 
 * ``qk_norm_rope`` -- fused Q/K RMSNorm + axial 3-D RoPE, in place
   (Sol-H3, arXiv 2609.35110, section 3.5 "Kernel Fusion", operator group 2).
+* ``qk_norm_rope_lora`` -- the same as a LoRA consumer: base + delta is
+  rounded to bf16 first (Sol-H3 section 3.5, precision-preserving LoRA fusion).
 * ``attention`` -- softmax(Q K^T * scale) V over packed sequences with a
   valid length, or over grouped query ranges with their own KV extents
   (vLLM-Omni blog section 3.1; SolarWM-H3 Realtime blog stage 2).
@@ -23,8 +25,8 @@ import torch
 
 from . import _binding
 
-__all__ = ["H3Error", "qk_norm_rope", "attention", "status_word", "lib", "HEAD_DIM",
-           "MAX_SEGMENTS", "attention_block"]
+__all__ = ["H3Error", "qk_norm_rope", "qk_norm_rope_lora", "attention", "status_word", "lib",
+           "HEAD_DIM", "MAX_SEGMENTS", "attention_block"]
 
 HEAD_DIM = 128
 MAX_SEGMENTS = 16
@@ -83,6 +85,33 @@ def qk_norm_rope(q: torch.Tensor, k: torch.Tensor, wq: torch.Tensor, wk: torch.T
                                  wk.data_ptr(), pos_thw.data_ptr(), int(n_rows), H, HEAD_DIM,
                                  int(rot[0]), int(rot[1]), int(rot[2]), float(theta),
                                  float(eps), _stream(stream)))
+
+
+def qk_norm_rope_lora(q: torch.Tensor, q_delta: torch.Tensor, k: torch.Tensor,
+                      k_delta: torch.Tensor, wq: torch.Tensor, wk: torch.Tensor,
+                      pos_thw: torch.Tensor, n_rows: Optional[int] = None,
+                      rot=(32, 48, 48), theta: float = 10000.0, eps: float = 1e-6,
+                      stream=None) -> None:
+    """In place on the base branches q, k: x = bf16(base + delta), then
+    RoPE(RMSNorm(x) * w), for rows [0, n_rows)."""
+    qs, ks = _row_stride(q, "q"), _row_stride(k, "k")
+    dqs, dks = _row_stride(q_delta, "q_delta"), _row_stride(k_delta, "k_delta")
+    H = q.shape[1]
+    if n_rows is None:
+        n_rows = q.shape[0]
+    if not (0 <= n_rows <= min(q.shape[0], k.shape[0], q_delta.shape[0], k_delta.shape[0],
+                               pos_thw.shape[0])):
+        raise ValueError("n_rows exceeds the tensors")
+    if pos_thw.dtype != torch.int32 or not pos_thw.is_contiguous() or pos_thw.shape[-1] != 3:
+        raise ValueError("pos_thw must be contiguous int32 [rows, 3]")
+    for w, name in ((wq, "wq"), (wk, "wk")):
+        if w.dtype != torch.bfloat16 or not w.is_contiguous() or tuple(w.shape) != (H, HEAD_DIM):
+            raise ValueError(f"{name} must be contiguous bf16 [{H}, {HEAD_DIM}]")
+    _check(lib().h3_qk_norm_rope_lora(q.data_ptr(), qs, q_delta.data_ptr(), dqs, k.data_ptr(), ks,
+                                      k_delta.data_ptr(), dks, wq.data_ptr(), wk.data_ptr(),
+                                      pos_thw.data_ptr(), int(n_rows), H, HEAD_DIM, int(rot[0]),
+                                      int(rot[1]), int(rot[2]), float(theta), float(eps),
+                                      _stream(stream)))
 
 
 def _i32_array(values: Sequence[int]):

@@ -60,16 +60,22 @@ int h3_version(void) { return 1 * 10000 + 0 * 100 + 0; }
 
 const char* h3_last_error(void) { return t_last_error.c_str(); }
 
-int h3_qk_norm_rope(void* q, int64_t q_row_stride, void* k, int64_t k_row_stride, const void* wq,
-                    const void* wk, const int32_t* pos_thw, int64_t n_rows, int n_heads,
-                    int head_dim, int rot_t, int rot_h, int rot_w, float theta, float eps,
-                    h3_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared checks and launch of the plain and LoRA-fused prologue.
+int norm_rope_entry(void* q, int64_t q_row_stride, void* k, int64_t k_row_stride,
+                    const void* dq, int64_t dq_row_stride, const void* dk, int64_t dk_row_stride,
+                    bool lora, const void* wq, const void* wk, const int32_t* pos_thw,
+                    int64_t n_rows, int n_heads, int head_dim, int rot_t, int rot_h, int rot_w,
+                    float theta, float eps, h3_stream_t stream) {
   if (n_rows < 0) return fail(H3_ERR_ARG, "n_rows must be >= 0 (got %lld)", (long long)n_rows);
   if (n_heads < 1) return fail(H3_ERR_ARG, "n_heads must be >= 1 (got %d)", n_heads);
   if (head_dim != h3::kHeadDim) return fail(H3_ERR_SHAPE, "head_dim must be 128 (got %d)", head_dim);
-  if (n_heads > h3::prologue_max_heads())
-    return fail(H3_ERR_SHAPE, "n_heads must be <= %d for the prologue (got %d)",
-                h3::prologue_max_heads(), n_heads);
+  if (n_heads > h3::prologue_max_heads(lora))
+    return fail(H3_ERR_SHAPE, "n_heads must be <= %d for this prologue (got %d)",
+                h3::prologue_max_heads(lora), n_heads);
   if (rot_t < 0 || rot_h < 0 || rot_w < 0 || (rot_t | rot_h | rot_w) & 1)
     return fail(H3_ERR_SHAPE, "rotary sections must be even and >= 0 (got %d/%d/%d)", rot_t, rot_h,
                 rot_w);
@@ -83,16 +89,22 @@ int h3_qk_norm_rope(void* q, int64_t q_row_stride, void* k, int64_t k_row_stride
   if (q_row_stride < width || k_row_stride < width)
     return fail(H3_ERR_SHAPE, "row strides (%lld, %lld) must be >= n_heads*128 = %lld",
                 (long long)q_row_stride, (long long)k_row_stride, (long long)width);
+  if (lora && (dq_row_stride < width || dk_row_stride < width))
+    return fail(H3_ERR_SHAPE, "delta row strides (%lld, %lld) must be >= n_heads*128 = %lld",
+                (long long)dq_row_stride, (long long)dk_row_stride, (long long)width);
   if (n_rows == 0) return H3_OK;
-  if (!q || !k || !wq || !wk || !pos_thw) return fail(H3_ERR_ARG, "null pointer argument");
+  if (!q || !k || !wq || !wk || !pos_thw || (lora && (!dq || !dk)))
+    return fail(H3_ERR_ARG, "null pointer argument");
   if (q == k) return fail(H3_ERR_ARG, "q and k must be distinct buffers");
-  if (!aligned16(q) || !aligned16(k) || !aligned16(wq) || !aligned16(wk))
-    return fail(H3_ERR_ALIGN, "q, k, wq, wk must be 16-byte aligned");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(wq) || !aligned16(wk) ||
+      (lora && (!aligned16(dq) || !aligned16(dk))))
+    return fail(H3_ERR_ALIGN, "tensor and weight pointers must be 16-byte aligned");
   if ((reinterpret_cast<uintptr_t>(pos_thw) & 3u) != 0)
     return fail(H3_ERR_ALIGN, "pos_thw must be 4-byte aligned");
-  if ((q_row_stride * 2) % 16 != 0 || (k_row_stride * 2) % 16 != 0)
+  if ((q_row_stride * 2) % 16 != 0 || (k_row_stride * 2) % 16 != 0 ||
+      (lora && ((dq_row_stride * 2) % 16 != 0 || (dk_row_stride * 2) % 16 != 0)))
     return fail(H3_ERR_ALIGN, "row strides must be multiples of 8 elements (16 bytes)");
-  if (n_rows > (int64_t(1) << 31) * 8)
+  if (n_rows > (int64_t(1) << 30))
     return fail(H3_ERR_SHAPE, "n_rows too large for one launch");
   int st = check_device();
   if (st != H3_OK) return st;
@@ -111,9 +123,39 @@ int h3_qk_norm_rope(void* q, int64_t q_row_stride, void* k, int64_t k_row_stride
   a.rot[2] = rot_w;
   a.theta = theta;
   a.eps = eps;
+  if (lora) {
+    a.dq = static_cast<const __nv_bfloat16*>(dq);
+    a.dk = static_cast<const __nv_bfloat16*>(dk);
+    a.dq_stride = dq_row_stride;
+    a.dk_stride = dk_row_stride;
+  }
   cudaError_t e = h3::launch_qk_norm_rope(a, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(H3_ERR_LAUNCH, "qk_norm_rope launch: %s", cudaGetErrorString(e));
   return H3_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int h3_qk_norm_rope(void* q, int64_t q_row_stride, void* k, int64_t k_row_stride, const void* wq,
+                    const void* wk, const int32_t* pos_thw, int64_t n_rows, int n_heads,
+                    int head_dim, int rot_t, int rot_h, int rot_w, float theta, float eps,
+                    h3_stream_t stream) {
+  return norm_rope_entry(q, q_row_stride, k, k_row_stride, nullptr, 0, nullptr, 0, false, wq, wk,
+                         pos_thw, n_rows, n_heads, head_dim, rot_t, rot_h, rot_w, theta, eps,
+                         stream);
+}
+
+int h3_qk_norm_rope_lora(void* q, int64_t q_row_stride, const void* q_delta,
+                         int64_t q_delta_row_stride, void* k, int64_t k_row_stride,
+                         const void* k_delta, int64_t k_delta_row_stride, const void* wq,
+                         const void* wk, const int32_t* pos_thw, int64_t n_rows, int n_heads,
+                         int head_dim, int rot_t, int rot_h, int rot_w, float theta, float eps,
+                         h3_stream_t stream) {
+  return norm_rope_entry(q, q_row_stride, k, k_row_stride, q_delta, q_delta_row_stride, k_delta,
+                         k_delta_row_stride, true, wq, wk, pos_thw, n_rows, n_heads, head_dim,
+                         rot_t, rot_h, rot_w, theta, eps, stream);
 }
 
 int h3_attention(const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,

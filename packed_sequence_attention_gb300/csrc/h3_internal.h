@@ -25,11 +25,14 @@ struct NormRopeArgs {
   int n_heads;
   int rot[3];
   float theta, eps;
+  const __nv_bfloat16* dq = nullptr;  // LoRA deltas (both null: plain prologue)
+  const __nv_bfloat16* dk = nullptr;
+  int64_t dq_stride = 0, dk_stride = 0;
 };
 // Validated arguments -> one launch on `stream`.
 cudaError_t launch_qk_norm_rope(const NormRopeArgs& a, cudaStream_t stream);
 // Largest n_heads the prologue's shared-memory ring holds.
-int prologue_max_heads();
+int prologue_max_heads(bool lora);
 // Device address of the status word on the current device (nullptr on error).
 uint32_t* status_word_device_ptr();
 

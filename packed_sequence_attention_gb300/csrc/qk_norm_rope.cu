@@ -41,6 +41,8 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 struct NormRopeParams {
   __nv_bfloat16* x[2];
   int64_t stride[2];
+  const __nv_bfloat16* d[2];  // LoRA branch outputs (delta) of Q and K, or null
+  int64_t dstride[2];
   const __nv_bfloat16* w[2];
   const int32_t* pos;
   uint32_t* status;
@@ -78,6 +80,10 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
+// kLora: the item is base + delta; the sum is rounded to bf16 first, as the
+// separate branches would store it (Sol-H3 section 3.5, precision-preserving
+// LoRA fusion), then normalised and rotated.
+template <bool kLora>
 __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_constant__ NormRopeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x;
@@ -87,7 +93,7 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_con
   constexpr int kSlots = kThreads / 8;
   const int H = p.n_heads;
   const uint32_t row_bytes = static_cast<uint32_t>(H) * kHeadDim * 2;
-  const uint32_t stage_bytes = row_bytes;  // one tensor row per item
+  const uint32_t stage_bytes = (kLora ? 2 : 1) * row_bytes;  // one tensor row (+ its delta row)
   const int NST = p.n_stages;
   const uint32_t sbase = smem_u32(smem);
   float2* tab = reinterpret_cast<float2*>(smem + NST * stage_bytes);  // [NST][64] (cos, sin)
@@ -120,6 +126,8 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_con
     const uint32_t bar = s_bar + 8 * s;
     mbar_arrive_expect_tx(bar, stage_bytes);
     bulk_load(sbase + s * stage_bytes, p.x[tt] + row * p.stride[tt], row_bytes, bar);
+    if (kLora)
+      bulk_load(sbase + s * stage_bytes + row_bytes, p.d[tt] + row * p.dstride[tt], row_bytes, bar);
   };
 
   if (tid == 0) {
@@ -177,6 +185,17 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_con
       if (live) {
         unpack8(lds128(src), x);
         unpack8(lds128(src + 128), x + 8);
+        if (kLora) {
+          float dx[16];
+          unpack8(lds128(src + row_bytes), dx);
+          unpack8(lds128(src + row_bytes + 128), dx + 8);
+#pragma unroll
+          for (int c = 0; c < 16; c += 2) {  // base + delta, rounded to bf16 (RNE)
+            const uint32_t r2 = pack_bf16x2(x[c] + dx[c], x[c + 1] + dx[c + 1]);
+            x[c] = __uint_as_float(r2 << 16);
+            x[c + 1] = __uint_as_float(r2 & 0xFFFF0000u);
+          }
+        }
       } else {
 #pragma unroll
         for (int c = 0; c < 16; ++c) x[c] = 0.0f;
@@ -218,10 +237,11 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_con
 
 }  // namespace
 
-int prologue_max_heads() {
-  // Two stages of one tensor row (256 B per head) plus two cos/sin tables and
-  // the barriers must fit in 227 KB of shared memory: 452 heads; keep 448.
-  return 448;
+int prologue_max_heads(bool lora) {
+  // Two stages of one tensor row (256 B per head; twice that with the LoRA
+  // delta row) plus two cos/sin tables and the barriers must fit in 227 KB of
+  // shared memory: 452 heads (225 with LoRA); keep 448 (220).
+  return lora ? 220 : 448;
 }
 
 cudaError_t launch_qk_norm_rope(const NormRopeArgs& a, cudaStream_t stream) {
@@ -260,32 +280,36 @@ cudaError_t launch_qk_norm_rope(const NormRopeArgs& a, cudaStream_t stream) {
     }
   }
   // Ring depth: two stages (one item in flight while one is processed).
-  const size_t stage_bytes = 1ull * a.n_heads * kHeadDim * 2;
+  const bool lora = a.dq != nullptr;
+  p.d[0] = a.dq;
+  p.d[1] = a.dk;
+  p.dstride[0] = a.dq_stride;
+  p.dstride[1] = a.dk_stride;
+  const size_t stage_bytes = (lora ? 2ull : 1ull) * a.n_heads * kHeadDim * 2;
   const int nst = 2;
   p.n_stages = nst;
   const size_t smem = nst * (stage_bytes + 64 * 8) + kMaxStages * 8;
-  static int attr_done[64];
-  static size_t attr_smem[64];
+  auto kernel = lora ? qk_norm_rope_kernel<true> : qk_norm_rope_kernel<false>;
+  static size_t attr_smem[2][64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_done[dev] || attr_smem[dev] < smem) {
-    e = cudaFuncSetAttribute(qk_norm_rope_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (attr_smem[lora][dev] < smem) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    attr_done[dev] = 1;
-    attr_smem[dev] = smem;
+    attr_smem[lora][dev] = smem;
   }
   int per_sm = 0, sms = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, qk_norm_rope_kernel, kThreads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem);
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
   int64_t grid = static_cast<int64_t>(sms) * per_sm;
   if (grid > 2 * a.n_rows) grid = 2 * a.n_rows;
-  qk_norm_rope_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(p);
+  kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -71,6 +71,30 @@ def test_norm_rope_zero_rows_is_a_no_op(lib):
     assert norm_rope(lib, n=0, q=None, k=None) == H3_OK
 
 
+def norm_rope_lora(lib, **kw):
+    a = dict(q=A, qs=5376, dq=A + 0x200000, dqs=5376, k=A + 0x100000, ks=5376, dk=A + 0x300000,
+             dks=5376, wq=A, wk=A, pos=A, n=10, H=42, D=128, rt=32, rh=48, rw=48, theta=10000.0,
+             eps=1e-6, stream=None)
+    a.update(kw)
+    return lib.h3_qk_norm_rope_lora(a["q"], a["qs"], a["dq"], a["dqs"], a["k"], a["ks"], a["dk"],
+                                    a["dks"], a["wq"], a["wk"], a["pos"], a["n"], a["H"], a["D"],
+                                    a["rt"], a["rh"], a["rw"], a["theta"], a["eps"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dq=None), ARG), (dict(dk=None), ARG), (dict(dq=A + 8), ALIGN), (dict(dks=5380), ALIGN),
+    (dict(dqs=100), SHAPE), (dict(H=221, qs=221 * 128, ks=221 * 128, dqs=221 * 128,
+                                  dks=221 * 128), SHAPE),
+    (dict(n=-1), ARG), (dict(D=64), SHAPE), (dict(k=A), ARG), (dict(rw=50), SHAPE),
+])
+def test_norm_rope_lora_rejects_on_host(lib, kw, code):
+    assert norm_rope_lora(lib, **kw) == code
+
+
+def test_norm_rope_lora_zero_rows_is_a_no_op(lib):
+    assert norm_rope_lora(lib, n=0, q=None, k=None, dq=None, dk=None) == H3_OK
+
+
 def attn(lib, **kw):
     a = dict(q=A, qs=5376, k=A, ks=5376, v=A, vs=5376, o=A + 0x100000, os=5376,
              cq=[0, 256], ckv=[0, 256], valid=[250], n_seq=None, H=42, D=128, scale=0.08838,
@@ -103,6 +127,7 @@ def test_attention_rejects_on_host(lib, kw, code):
 def test_valid_call_without_gpu_reports_device_error(lib):
     assert attn(lib) == DEVICE
     assert norm_rope(lib) == DEVICE
+    assert norm_rope_lora(lib) == DEVICE
     v = ctypes.c_uint32(0)
     assert lib.h3_status_word(ctypes.byref(v)) == DEVICE
 

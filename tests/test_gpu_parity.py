@@ -128,6 +128,47 @@ def test_prologue_head_counts(H, rows):
         prologue_bound(got, ref)
 
 
+@pytest.mark.parametrize("name", ["tiny", "medium"])
+def test_lora_prologue_matches_separate_branches_bitwise(name):
+    # The pages' claim for the fused LoRA consumer: byte-exact against the
+    # native path that adds the branches into a bf16 tensor first.
+    inp = W.make_inputs(name, device="cuda")
+    w = inp["workload"]
+    n = w.segments[0].n_valid_q()
+    gen = torch.Generator(device="cuda").manual_seed(123)
+    dq = (0.05 * torch.randn(inp["q"].shape, generator=gen, device="cuda")).to(torch.bfloat16)
+    dk = (0.05 * torch.randn(inp["k"].shape, generator=gen, device="cuda")).to(torch.bfloat16)
+    q0, k0 = inp["q"].clone(), inp["k"].clone()
+    qf, kf = inp["q"].clone(), inp["k"].clone()
+    h3.qk_norm_rope_lora(qf, dq, kf, dk, inp["wq"], inp["wk"], inp["pos_thw"], n_rows=n, rot=ROT)
+    qs, ks = q0 + dq, k0 + dk  # the separate branches: bf16 sum stored, then the prologue
+    h3.qk_norm_rope(qs, ks, inp["wq"], inp["wk"], inp["pos_thw"], n_rows=n, rot=ROT)
+    torch.cuda.synchronize()
+    assert torch.equal(qf[:n].view(torch.int16), qs[:n].view(torch.int16))
+    assert torch.equal(kf[:n].view(torch.int16), ks[:n].view(torch.int16))
+    assert torch.equal(qf[n:].view(torch.int16), q0[n:].view(torch.int16))  # rows past n untouched
+    pos = inp["pos_thw"].cpu().numpy()[:n]
+    for base, delta, wn, got in ((q0, dq, "wq", qf), (k0, dk, "wk", kf)):
+        ref = O.qk_norm_rope_lora(O.widen(base[:n]), O.widen(delta[:n]), O.widen(inp[wn]), pos)
+        gate(O.widen(got[:n]), ref, f"lora {name}")
+        prologue_bound(O.widen(got[:n]), ref)
+
+
+def test_lora_prologue_strided_views():
+    inp = W.make_inputs("medium", device="cuda", packed_qkv=True)
+    n = 4000
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    dbuf = (0.1 * torch.randn((4096, 2, 42, 128), generator=gen, device="cuda")).to(torch.bfloat16)
+    dq, dk = dbuf[:, 0], dbuf[:, 1]
+    q0, k0 = inp["q"].clone(), inp["k"].clone()
+    h3.qk_norm_rope_lora(inp["q"], dq, inp["k"], dk, inp["wq"], inp["wk"], inp["pos_thw"], n_rows=n)
+    torch.cuda.synchronize()
+    pos = inp["pos_thw"].cpu().numpy()[:n]
+    for base, delta, wn, got in ((q0, dq, "wq", inp["q"]), (k0, dk, "wk", inp["k"])):
+        ref = O.qk_norm_rope_lora(O.widen(base[:n]), O.widen(delta[:n]), O.widen(inp[wn]), pos)
+        gate(O.widen(got[:n]), ref, "lora strided")
+
+
 def test_prologue_full_size_sampled():
     inp = W.make_inputs("full", device="cuda")
     q0, k0 = inp["q"].cpu(), inp["k"].cpu()

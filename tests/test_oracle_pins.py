@@ -241,6 +241,40 @@ def pin_softmax_rows(Ox):
     return max(worst, float(np.max(np.abs(ratio))))
 
 
+def pin_round_bf16(Ox):
+    """bf16 rounding: hand-derived ties and overflow, fp32-exact values
+    against torch's own fp32 -> bf16 conversion."""
+    cases = {1.0 + 2.0 ** -8: 1.0, 1.0 + 3 * 2.0 ** -8: 1.0 + 2.0 ** -6,
+             1.0 + 2.0 ** -8 + 2.0 ** -30: 1.0 + 2.0 ** -7, -(1.0 + 2.0 ** -8): -1.0,
+             3.0e38: 2.0 ** 127 * (226 / 128), 3.4e38: math.inf, 0.0: 0.0,
+             2.0 ** -140: 2.0 ** -140 if 2.0 ** -140 >= 2.0 ** -133 else 0.0}
+    worst = 0.0
+    for x, want in cases.items():
+        got = float(Ox.round_bf16(np.array([x]))[0])
+        worst = max(worst, 0.0 if got == want else 1.0)
+    x = np.random.default_rng(8).standard_normal(20000).astype(np.float32).astype(np.float64) * 37.0
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    worst = max(worst, float(np.max(np.abs(Ox.round_bf16(x) - ref))))
+    return worst
+
+
+def pin_lora_prologue(Ox):
+    """delta = 0 reduces to the plain prologue; otherwise the fused result is
+    the prologue of the bf16-rounded sum, checked against the brute force."""
+    inp, f = _tiny_inputs()
+    pos = inp["pos_thw"].numpy()
+    z = Ox.qk_norm_rope_lora(f["q"], np.zeros_like(f["q"]), f["wq"], pos, SECTIONS, THETA, EPS)
+    worst = float(np.max(np.abs(z - Ox.qk_norm_rope(f["q"], f["wq"], pos, SECTIONS, THETA, EPS))))
+    delta = np.random.default_rng(9).standard_normal(f["q"].shape) * 0.05
+    got = Ox.qk_norm_rope_lora(f["q"], delta, f["wq"], pos, SECTIONS, THETA, EPS)
+    for r in (0, 100, 200, 249):
+        for h in range(2):
+            exp = brute.norm_rope_lora_row(list(f["q"][r, h]), list(delta[r, h]), list(f["wq"][h]),
+                                           tuple(int(v) for v in pos[r]), SECTIONS, THETA, EPS)
+            worst = max(worst, float(np.max(np.abs(got[r, h] - np.array(exp)))))
+    return worst
+
+
 PINS = [
     (pin_norm_closed_form, 1e-12),
     (pin_norm_scale_invariance, 1e-12),
@@ -253,6 +287,8 @@ PINS = [
     (pin_attention_grouped_sdpa, 1e-12),
     (pin_attention_invariants, 1e-12),
     (pin_softmax_rows, 1e-9),
+    (pin_round_bf16, 0.0),
+    (pin_lora_prologue, 1e-12),
 ]
 
 
@@ -281,6 +317,11 @@ def _mutant(**overrides):
             O.softmax_rows = saved
     if "qk_norm_rope" not in overrides:
         ns.qk_norm_rope = qk_norm_rope
+
+    def qk_norm_rope_lora(base, delta, w, pos, sections=SECTIONS, theta=THETA, eps=EPS):
+        return ns.qk_norm_rope(ns.round_bf16(base + delta), w, pos, sections, theta, eps)
+    if "qk_norm_rope_lora" not in overrides:
+        ns.qk_norm_rope_lora = qk_norm_rope_lora
     ns.attention = attention
     return ns
 
@@ -350,6 +391,24 @@ def _attn_pad_keys(q, k, v, cu_q, cu_kv, vl, scale, rows=None):
     return O.attention(q, np.nan_to_num(k), np.nan_to_num(v), cu_q, cu_kv, None, scale, rows)
 
 
+def _round_trunc(x):
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)
+    q = np.ldexp(1.0, e - 8)
+    return np.trunc(x / q) * q
+
+
+def _round_half_up(x):
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)
+    q = np.ldexp(1.0, e - 8)
+    return np.floor(x / q + 0.5) * q
+
+
+def _lora_no_round(base, delta, w, pos, sections=SECTIONS, theta=THETA, eps=EPS):
+    return O.qk_norm_rope(base + delta, w, pos, sections, theta, eps)
+
+
 MUTANTS = {
     "rope_sign_flip": dict(rope_axial=_rope_sign_flip),
     "rope_rotate_half": dict(rope_axial=_rope_rotate_half),
@@ -362,6 +421,9 @@ MUTANTS = {
     "attn_transposed": dict(attention=_attn_transposed),
     "attn_no_scale": dict(attention=_attn_no_scale),
     "attn_pad_keys": dict(attention=_attn_pad_keys),
+    "round_truncates": dict(round_bf16=_round_trunc),
+    "round_half_up": dict(round_bf16=_round_half_up),
+    "lora_skips_rounding": dict(qk_norm_rope_lora=_lora_no_round),
 }
 
 
