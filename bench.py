@@ -229,6 +229,7 @@ def bench_gpu(args):
         pro_alone_ms = a0.elapsed_time(a1) / 10
     pro_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs])) if w.self_attention else 0.0
     lora = lora_prologue_timing(h3, g, w, stream, pk) if w.self_attention else None
+    ref_cached = ref_cached_timing(h3, W, stream, pk) if w.name == "full" else None
     status = h3.status_word()
     if status:
         raise SystemExit(f"device status word {status:#x} after the timed region")
@@ -333,7 +334,7 @@ def bench_gpu(args):
         "prologue_alone_us": round(pro_alone_ms * 1e3, 2) if pro_alone_ms else None,
         "prologue_alone_gbs": round(w.prologue_bytes() / (pro_alone_ms * 1e-3) / 1e9, 1)
         if pro_alone_ms else None,
-        "next_rows": {"lora_prologue": lora},
+        "next_rows": {"lora_prologue": lora, "ref_cached_attention": ref_cached},
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 3)},
         "gpu_launches": launches_per_step(w) * args.steps,
@@ -391,6 +392,29 @@ def lora_prologue_timing(h3, g, w, stream, pk, iters=10):
             "frac_hbm_measured": round(nbytes / us / 1e3 / pk["hbm"], 4),
             "bytes": nbytes, "separate_branches_us": round(sep, 2),
             "speedup_vs_separate": round(sep / us, 3)}
+
+
+def ref_cached_timing(h3, W, stream, pk, iters=5):
+    """Attention of a reference-to-video step after the first: 16,422 current
+    queries over the cached K/V of 3 reference videos (42,336 rows) plus the
+    current K/V (16,422 rows), through h3_attention_groups."""
+    inp = W.ref_cached_inputs(device=f"cuda:{torch.cuda.current_device()}")
+
+    def run():
+        h3.attention_groups(inp["q"], inp["k"], inp["v"], inp["groups"], inp["k_cache"],
+                            inp["v_cache"], SCALE, out=inp["out"])
+    run()
+    torch.cuda.synchronize()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(iters):
+        run()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    ms = a0.elapsed_time(a1) / iters
+    tf = inp["flops"] / (ms * 1e-3) / 1e12
+    return {"ms": round(ms, 3), "tflops": round(tf, 1), "frac_of_burst": round(tf / pk["bf16"], 4),
+            "queries": 16422, "keys": 16422 + 42336, "flop": inp["flops"]}
 
 
 def committed_traffic(w):

@@ -155,6 +155,46 @@ int h3_attention(const void* q, int64_t q_row_stride, const void* k, int64_t k_r
                  const int32_t* valid_len, int n_seq, int n_heads, int head_dim,
                  float scale, h3_stream_t stream);
 
+/*
+ * h3_attention_groups -- query groups over KV views, including a cached KV
+ * range, in one launch.
+ *
+ * Follows the reference KV caching of Sol-H3 (section 5, Fig. 4): after the
+ * first denoising step the reference query rows are skipped and the text /
+ * generation queries attend to the cached reference K/V together with the
+ * current tokens' K/V; and the history K/V reuse of the SolarWM-H3 Realtime
+ * blog (stage 3), where query groups read a pre-concatenated history.
+ *
+ * Group g: query rows [q_start, q_start + q_len) of q and out attend to the
+ * union of k / v rows [kv_start, kv_start + kv_len) and k_cache / v_cache
+ * rows [cache_start, cache_start + cache_len):
+ *   out[i, h] = sum_j softmax_j(scale * <q[i, h], key_j[h]>) value_j[h]
+ * KV views may overlap between groups; query ranges must not.  Output rows
+ * that belong to no group (for instance skipped reference queries) are not
+ * written; a group whose two views are both empty writes zeros.
+ *
+ * q, out          device bf16 [rows, n_heads, 128]
+ * k, v            device bf16, rows as addressed by kv_start/kv_len
+ * k_cache, v_cache device bf16, rows as addressed by cache_start/cache_len;
+ *                 may be NULL when every cache_len is 0
+ * groups          HOST array of n_groups entries, 1 <= n_groups <= H3_MAX_SEGMENTS;
+ *                 all fields >= 0, start + len < 2^31.
+ * The caller guarantees that every addressed row exists.  Alignment, scale
+ * and error rules as h3_attention.
+ */
+typedef struct {
+  int32_t q_start, q_len;
+  int32_t kv_start, kv_len;
+  int32_t cache_start, cache_len;
+} h3_attn_group;
+
+int h3_attention_groups(const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,
+                        const void* v, int64_t v_row_stride, const void* k_cache,
+                        int64_t k_cache_row_stride, const void* v_cache,
+                        int64_t v_cache_row_stride, void* out, int64_t out_row_stride,
+                        const h3_attn_group* groups, int n_groups, int n_heads, int head_dim,
+                        float scale, h3_stream_t stream);
+
 /* Message for the last nonzero status returned to the calling thread
  * ("" if none).  The pointer stays valid until the thread's next call. */
 const char* h3_last_error(void);

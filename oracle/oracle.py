@@ -20,6 +20,11 @@ What is computed, with the passage each step follows:
   Sol-H3 section 3.2 "Optimized attention collectives", and the grouped
   condition / audio / video query ranges of the SolarWM-H3 Realtime blog,
   stage 2 "Attention Backend".
+* ``attention_groups`` -- query groups over KV views into the current K/V
+  and a cached K/V range (Sol-H3 reference KV caching, Fig. 4; SolarWM
+  history K/V reuse).
+* ``qk_norm_rope_lora`` / ``round_bf16`` -- the LoRA consumer fusion of
+  Sol-H3 section 3.5 (base + delta rounded to bf16 before the prologue).
 
 Readings taken where the pages are silent (each listed in the design notes):
 RMSNorm per head (128 channels) with weight [H, 128]; eps inside the root;
@@ -170,6 +175,47 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray,
                 s = scale * (q[rows[idx], h, :] @ kb.T)
                 out[idx, h, :] = softmax_rows(s) @ vb
     return out
+
+
+def attention_groups(q: np.ndarray, k: np.ndarray, v: np.ndarray,
+                     k_cache: np.ndarray, v_cache: np.ndarray, groups, scale: float,
+                     rows=None, block: int = 256) -> np.ndarray:
+    """Query groups over KV views, with a cached KV range (Sol-H3 section 5,
+    reference KV caching, Fig. 4: after the first step the reference query
+    rows are skipped and the remaining queries attend to the cached
+    reference K/V and to the current tokens' K/V; SolarWM-H3 Realtime blog,
+    stage 3: pre-concatenated history K/V reused across denoising forwards).
+
+    ``groups`` is a sequence of (q_start, q_len, kv_start, kv_len,
+    cache_start, cache_len): query rows [q_start, q_start + q_len) attend to
+    k/v rows [kv_start, kv_start + kv_len) together with k_cache/v_cache rows
+    [cache_start, cache_start + cache_len).  Views may overlap between
+    groups.  Returns (rows, out_rows): the query rows that belong to some
+    group (all of them, or those listed in ``rows``) and their outputs; a
+    group with no key at all outputs zeros.
+    """
+    H, D = q.shape[1], q.shape[2]
+    sel_rows, outs = [], []
+    for (q0, nq, k0, nk, c0, nc) in groups:
+        grp_rows = np.arange(q0, q0 + nq)
+        if rows is not None:
+            grp_rows = grp_rows[np.isin(grp_rows, rows)]
+        if grp_rows.size == 0:
+            continue
+        o = np.zeros((grp_rows.size, H, D))
+        if nk + nc > 0:
+            kk = np.concatenate([k[k0:k0 + nk], k_cache[c0:c0 + nc]], axis=0)
+            vv = np.concatenate([v[k0:k0 + nk], v_cache[c0:c0 + nc]], axis=0)
+            for h in range(H):
+                for i in range(0, grp_rows.size, block):
+                    r = grp_rows[i:i + block]
+                    s = scale * (q[r, h, :] @ kk[:, h, :].T)
+                    o[i:i + block, h, :] = softmax_rows(s) @ vv[:, h, :]
+        sel_rows.append(grp_rows)
+        outs.append(o)
+    if not outs:
+        return np.zeros(0, dtype=np.int64), np.zeros((0, H, D))
+    return np.concatenate(sel_rows), np.concatenate(outs, axis=0)
 
 
 def attention_flops(cu_seqlens_q, cu_seqlens_kv, valid_len, n_heads: int,

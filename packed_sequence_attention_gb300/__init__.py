@@ -11,6 +11,9 @@ strides and the current stream:
 * ``attention`` -- softmax(Q K^T * scale) V over packed sequences with a
   valid length, or over grouped query ranges with their own KV extents
   (vLLM-Omni blog section 3.1; SolarWM-H3 Realtime blog stage 2).
+* ``attention_groups`` -- query groups over KV views into the current K/V
+  plus a cached K/V range (Sol-H3 reference KV caching, Fig. 4; SolarWM
+  history K/V reuse).
 
 There is no CPU or library fallback: without the built library, or off an
 sm_103 device, every call raises ``H3Error``.
@@ -25,8 +28,8 @@ import torch
 
 from . import _binding
 
-__all__ = ["H3Error", "qk_norm_rope", "qk_norm_rope_lora", "attention", "status_word", "lib",
-           "HEAD_DIM", "MAX_SEGMENTS", "attention_block"]
+__all__ = ["H3Error", "qk_norm_rope", "qk_norm_rope_lora", "attention", "attention_groups",
+           "status_word", "lib", "HEAD_DIM", "MAX_SEGMENTS", "attention_block"]
 
 HEAD_DIM = 128
 MAX_SEGMENTS = 16
@@ -145,6 +148,41 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                               ctypes.cast(cq, _binding.c_i32p), ctypes.cast(ckv, _binding.c_i32p),
                               ctypes.cast(vl, _binding.c_i32p) if vl is not None else None,
                               n_seq, H, HEAD_DIM, float(scale), _stream(stream)))
+    return out
+
+
+def attention_groups(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, groups,
+                     k_cache: Optional[torch.Tensor] = None,
+                     v_cache: Optional[torch.Tensor] = None, scale: Optional[float] = None,
+                     out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Query groups over KV views plus an optional cached KV range.
+
+    ``groups``: sequence of (q_start, q_len, kv_start, kv_len, cache_start,
+    cache_len).  Rows of ``out`` outside every group are left untouched."""
+    H = q.shape[1]
+    if out is None:
+        out = torch.empty((q.shape[0], H, HEAD_DIM), dtype=torch.bfloat16, device=q.device)
+    tensors = [(q, "q"), (k, "k"), (v, "v"), (out, "out")]
+    uses_cache = any(g[5] > 0 for g in groups)
+    if uses_cache:
+        if k_cache is None or v_cache is None:
+            raise ValueError("a group uses the cache but k_cache / v_cache are missing")
+        tensors += [(k_cache, "k_cache"), (v_cache, "v_cache")]
+    strides = {n: _row_stride(t, n) for t, n in tensors}
+    for (q0, nq, k0, nk, c0, nc) in groups:
+        if q0 + nq > min(q.shape[0], out.shape[0]) or k0 + nk > min(k.shape[0], v.shape[0]) or \
+                (nc and c0 + nc > min(k_cache.shape[0], v_cache.shape[0])):
+            raise ValueError("a group addresses rows past the tensors")
+    arr = (_binding.AttnGroup * len(groups))(*[_binding.AttnGroup(*map(int, g)) for g in groups])
+    if scale is None:
+        scale = 1.0 / math.sqrt(HEAD_DIM)
+    kc_ptr = k_cache.data_ptr() if uses_cache else None
+    vc_ptr = v_cache.data_ptr() if uses_cache else None
+    _check(lib().h3_attention_groups(
+        q.data_ptr(), strides["q"], k.data_ptr(), strides["k"], v.data_ptr(), strides["v"],
+        kc_ptr, strides.get("k_cache", 0), vc_ptr, strides.get("v_cache", 0),
+        out.data_ptr(), strides["out"], ctypes.cast(arr, ctypes.c_void_p), len(groups), H,
+        HEAD_DIM, float(scale), _stream(stream)))
     return out
 
 

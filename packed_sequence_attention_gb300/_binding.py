@@ -11,6 +11,13 @@ _LOCK = threading.Lock()
 _LIB = None
 
 c_int, c_int64, c_float, c_void_p = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
+
+
+class AttnGroup(ctypes.Structure):
+    """h3_attn_group: one query group and its two KV views."""
+    _fields_ = [("q_start", ctypes.c_int32), ("q_len", ctypes.c_int32),
+                ("kv_start", ctypes.c_int32), ("kv_len", ctypes.c_int32),
+                ("cache_start", ctypes.c_int32), ("cache_len", ctypes.c_int32)]
 c_i32p = ctypes.POINTER(ctypes.c_int32)
 c_u32p = ctypes.POINTER(ctypes.c_uint32)
 
@@ -27,6 +34,9 @@ SIGNATURES = {
     "h3_attention": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_int64,
                              c_void_p, c_int64, c_i32p, c_i32p, c_i32p, c_int, c_int, c_int,
                              c_float, c_void_p]),
+    "h3_attention_groups": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_int64,
+                                    c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_int64,
+                                    c_void_p, c_int, c_int, c_int, c_float, c_void_p]),
     "h3_last_error": (ctypes.c_char_p, []),
     "h3_status_word": (c_int, [c_u32p]),
     "h3_version": (c_int, []),

@@ -1,6 +1,7 @@
 // C-ABI front end of libh3kern: argument checks on the host, device checks,
 // then one launch per call.  See include/h3kern.h for the contract.
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -213,6 +214,77 @@ int h3_attention(const void* q, int64_t q_row_stride, const void* k, int64_t k_r
   a.scale = scale;
   std::string err;
   st = h3::launch_attention(a, reinterpret_cast<cudaStream_t>(stream), err);
+  if (st != H3_OK) return fail(st, "%s", err.c_str());
+  return H3_OK;
+}
+
+int h3_attention_groups(const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,
+                        const void* v, int64_t v_row_stride, const void* k_cache,
+                        int64_t k_cache_row_stride, const void* v_cache,
+                        int64_t v_cache_row_stride, void* out, int64_t out_row_stride,
+                        const h3_attn_group* groups, int n_groups, int n_heads, int head_dim,
+                        float scale, h3_stream_t stream) {
+  if (n_groups < 1 || n_groups > H3_MAX_SEGMENTS)
+    return fail(H3_ERR_ARG, "n_groups must be in [1, %d] (got %d)", H3_MAX_SEGMENTS, n_groups);
+  if (!groups) return fail(H3_ERR_ARG, "null groups");
+  if (n_heads < 1) return fail(H3_ERR_ARG, "n_heads must be >= 1 (got %d)", n_heads);
+  if (head_dim != h3::kHeadDim) return fail(H3_ERR_SHAPE, "head_dim must be 128 (got %d)", head_dim);
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return fail(H3_ERR_ARG, "scale must be finite and > 0");
+  bool uses_cache = false;
+  for (int g = 0; g < n_groups; ++g) {
+    const h3_attn_group& G = groups[g];
+    const int64_t f[6] = {G.q_start, G.q_len, G.kv_start, G.kv_len, G.cache_start, G.cache_len};
+    for (int i = 0; i < 6; ++i)
+      if (f[i] < 0) return fail(H3_ERR_ARG, "group %d has a negative field", g);
+    if (f[0] + f[1] > INT32_MAX || f[2] + f[3] > INT32_MAX || f[4] + f[5] > INT32_MAX)
+      return fail(H3_ERR_ARG, "group %d addresses rows past 2^31", g);
+    uses_cache = uses_cache || G.cache_len > 0;
+    for (int o = 0; o < g; ++o) {  // query ranges must not overlap (racing writes)
+      const h3_attn_group& P = groups[o];
+      if (G.q_len > 0 && P.q_len > 0 && G.q_start < P.q_start + P.q_len &&
+          P.q_start < G.q_start + G.q_len)
+        return fail(H3_ERR_ARG, "query ranges of groups %d and %d overlap", o, g);
+    }
+  }
+  const int64_t width = static_cast<int64_t>(n_heads) * h3::kHeadDim;
+  if (q_row_stride < width || k_row_stride < width || v_row_stride < width ||
+      out_row_stride < width || (uses_cache && (k_cache_row_stride < width ||
+                                                v_cache_row_stride < width)))
+    return fail(H3_ERR_SHAPE, "row strides must be >= n_heads*128 = %lld", (long long)width);
+  if (!q || !k || !v || !out || (uses_cache && (!k_cache || !v_cache)))
+    return fail(H3_ERR_ARG, "null tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (uses_cache && (!aligned16(k_cache) || !aligned16(v_cache))))
+    return fail(H3_ERR_ALIGN, "tensor pointers must be 16-byte aligned");
+  if ((q_row_stride * 2) % 16 || (k_row_stride * 2) % 16 || (v_row_stride * 2) % 16 ||
+      (out_row_stride * 2) % 16 ||
+      (uses_cache && ((k_cache_row_stride * 2) % 16 || (v_cache_row_stride * 2) % 16)))
+    return fail(H3_ERR_ALIGN, "row strides must be multiples of 8 elements (16 bytes)");
+  const int64_t lim = int64_t(1) << 40;
+  if (q_row_stride * 2 >= lim || k_row_stride * 2 >= lim || v_row_stride * 2 >= lim ||
+      k_cache_row_stride * 2 >= lim || v_cache_row_stride * 2 >= lim)
+    return fail(H3_ERR_SHAPE, "row stride too large for a tensor map");
+  int st = check_device();
+  if (st != H3_OK) return st;
+  h3::AttnGroupArgs a{};
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k = static_cast<const __nv_bfloat16*>(k);
+  a.v = static_cast<const __nv_bfloat16*>(v);
+  a.kc = static_cast<const __nv_bfloat16*>(k_cache);
+  a.vc = static_cast<const __nv_bfloat16*>(v_cache);
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.q_stride = q_row_stride;
+  a.k_stride = k_row_stride;
+  a.v_stride = v_row_stride;
+  a.kc_stride = k_cache_row_stride;
+  a.vc_stride = v_cache_row_stride;
+  a.out_stride = out_row_stride;
+  a.groups = groups;
+  a.n_groups = n_groups;
+  a.n_heads = n_heads;
+  a.scale = scale;
+  std::string err;
+  st = h3::launch_attention_groups(a, reinterpret_cast<cudaStream_t>(stream), err);
   if (st != H3_OK) return fail(st, "%s", err.c_str());
   return H3_OK;
 }

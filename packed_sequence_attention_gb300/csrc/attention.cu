@@ -85,16 +85,18 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kHeadDim, false, true);  // V 
 struct Seg {
   int32_t q_row0;   // first row of the segment in q / out
   int32_t nq;       // valid query rows (> 0)
-  int32_t nkv;      // valid key rows (> 0)
+  int32_t nkv;      // key rows of the first KV view (k / v)
+  int32_t nkv2;     // key rows of the second KV view (k_cache / v_cache), may be 0
   int32_t n_pairs;  // ceil(nq / 256)
   int32_t cta0;     // first CTA of the segment
-  int32_t pad_;
 };
 
 struct __align__(128) AttnParams {
   CUtensorMap tm_q[H3_MAX_SEGMENTS];
-  CUtensorMap tm_k[H3_MAX_SEGMENTS];
+  CUtensorMap tm_k[H3_MAX_SEGMENTS];   // first KV view
   CUtensorMap tm_v[H3_MAX_SEGMENTS];
+  CUtensorMap tm_k2[H3_MAX_SEGMENTS];  // second KV view (cached keys), if any
+  CUtensorMap tm_v2[H3_MAX_SEGMENTS];
   Seg seg[H3_MAX_SEGMENTS];  // schedule order (longest KV first)
   int32_t zero_row0[H3_MAX_SEGMENTS];
   int32_t zero_rows[H3_MAX_SEGMENTS];
@@ -221,7 +223,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const int head = local / sg.n_pairs;
   const int qrow0 = (local - head * sg.n_pairs) * (2 * kBM);  // segment-relative
   const int n_tiles = (qrow0 + kBM < sg.nq) ? 2 : 1;
-  const int n_kv = (sg.nkv + kBN - 1) / kBN;
+  // KV tiles: those of the first view, then those of the second; the online
+  // softmax does not depend on the order in which keys are visited.
+  const int n_kv1 = (sg.nkv + kBN - 1) / kBN;
+  const int n_kv = n_kv1 + (sg.nkv2 + kBN - 1) / kBN;
 
   // ---- set-up: barriers (thread 0), TMEM (warp 9)
   if (threadIdx.x == 0) {
@@ -254,11 +259,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     // ================================================= TMA producer
     if (lane == 0 && *abort_flag == 0u) {
       const CUtensorMap* tq = &p.tm_q[si];
-      const CUtensorMap* tk = &p.tm_k[si];
-      const CUtensorMap* tv = &p.tm_v[si];
+      const CUtensorMap* tk1 = &p.tm_k[si];
+      const CUtensorMap* tv1 = &p.tm_v[si];
+      const CUtensorMap* tk2 = &p.tm_k2[si];
+      const CUtensorMap* tv2 = &p.tm_v2[si];
       prefetch_tmap(tq);
-      prefetch_tmap(tk);
-      prefetch_tmap(tv);
+      prefetch_tmap(tk1);
+      prefetch_tmap(tv1);
+      if (sg.nkv2 > 0) {
+        prefetch_tmap(tk2);
+        prefetch_tmap(tv2);
+      }
       mbar_arrive_expect_tx(bar(BAR_Q), n_tiles * kTileBytes);
       for (int t = 0; t < n_tiles; ++t)
         for (int h = 0; h < 2; ++h)
@@ -272,14 +283,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (j >= kNS) ok = wait1(bar(BAR_KVEMPTY + s), (use - 1) & 1, wctx, H3_STATUS_TIMEOUT_LOAD);
         if (!ok) break;
         if (p.fault == 1 && j == 1) continue;  // test hook: leave this stage empty
+        const bool first = j < n_kv1;
+        const CUtensorMap* tk = first ? tk1 : tk2;
+        const CUtensorMap* tv = first ? tv1 : tv2;
+        const int row = (first ? j : j - n_kv1) * kBN;
         mbar_arrive_expect_tx(bar(BAR_KFULL + s), kTileBytes);
         for (int h = 0; h < 2; ++h)
           tma_load_3d(sbase + kOffK + s * kTileBytes + h * kHalfBytes, tk, bar(BAR_KFULL + s),
-                      h * 64, head, j * kBN);
+                      h * 64, head, row);
         mbar_arrive_expect_tx(bar(BAR_VFULL + s), kTileBytes);
         for (int h = 0; h < 2; ++h)
           tma_load_3d(sbase + kOffV + s * kTileBytes + h * kHalfBytes, tv, bar(BAR_VFULL + s),
-                      h * 64, head, j * kBN);
+                      h * 64, head, row);
         armed[s] = use;
       }
       if (*abort_flag != 0u) {
@@ -364,7 +379,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const uint32_t tS = tmem + lane_base + kColS + t * 128;
       const uint32_t tO = tmem + lane_base + kColO + t * 128;
       const float c = p.scale_log2;
-      const int kv_tail = sg.nkv - (n_kv - 1) * kBN;  // valid columns of the last tile
+      // valid columns of the last tile of each view (128 when it is full)
+      const int tail1 = sg.nkv - (n_kv1 - 1) * kBN;
+      const int tail2 = sg.nkv2 - (n_kv - n_kv1 - 1) * kBN;
       float m_used = -INFINITY;
       float l = 0.0f;
       bool ok = true;
@@ -377,7 +394,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, s[q]);
 #pragma unroll
         for (int q = 0; q < 4; ++q) tmem_wait_ld(s[q]);
-        if (j == n_kv - 1 && kv_tail < kBN) {
+        const int kv_tail = (j == n_kv1 - 1) ? tail1 : (j == n_kv - 1) ? tail2 : kBN;
+        if (kv_tail < kBN) {
 #pragma unroll
           for (int q = 0; q < 4; ++q)
 #pragma unroll
@@ -528,51 +546,71 @@ std::atomic<int> g_fault_next{0};
 
 }  // namespace
 
-int launch_attention(const AttnArgs& a, cudaStream_t stream, std::string& err) {
+namespace {
+
+struct Item {
+  int q0, nq;  // query rows
+  int kv0, nkv;  // first KV view: rows of k / v
+  int c0, nc;    // second KV view: rows of k_cache / v_cache
+};
+
+struct Buffers {
+  const __nv_bfloat16 *q, *k, *v, *kc, *vc;
+  __nv_bfloat16* out;
+  int64_t q_stride, k_stride, v_stride, kc_stride, vc_stride, out_stride;
+};
+
+// Work items (at most H3_MAX_SEGMENTS, nq > 0, nkv + nc > 0) and output
+// row ranges to zero -> tensor maps, schedule, one launch.
+int launch_items(const Buffers& b, std::vector<Item>& items,
+                 const std::vector<std::pair<int, int>>& zero, int n_heads, float scale,
+                 cudaStream_t stream, std::string& err) {
   EncodeTiledFn enc = get_encoder(err);
   if (!enc) return H3_ERR_DEVICE;
-  thread_local AttnParams P;  // ~6.7 KB of kernel parameters, rebuilt on every call
+  thread_local AttnParams P;  // ~11 KB of kernel parameters, rebuilt on every call
   std::memset(&P, 0, sizeof(P));
-
-  struct Item {
-    int b, q0, nq, kv0, nkv;
-  };
-  std::vector<Item> items;
   P.n_zero = 0;
   P.zero_chunks = 0;
-  for (int b = 0; b < a.n_seq; ++b) {
-    const int q0 = a.cu_q[b], q_ext = a.cu_q[b + 1] - a.cu_q[b];
-    const int kv0 = a.cu_kv[b], kv_ext = a.cu_kv[b + 1] - a.cu_kv[b];
-    int nq = a.valid ? a.valid[b] : q_ext;
-    const int nkv = a.valid ? a.valid[b] : kv_ext;
-    if (nkv == 0) nq = 0;  // no key: every query row of the segment is 0
-    if (nq > 0) items.push_back({b, q0, nq, kv0, nkv});
-    if (q_ext > nq) {
-      P.zero_row0[P.n_zero] = q0 + nq;
-      P.zero_rows[P.n_zero] = q_ext - nq;
-      P.zero_chunks += static_cast<int64_t>(q_ext - nq) * a.n_heads * 16;
-      ++P.n_zero;
-    }
+  for (const auto& z : zero) {
+    if (z.second <= 0) continue;
+    P.zero_row0[P.n_zero] = z.first;
+    P.zero_rows[P.n_zero] = z.second;
+    P.zero_chunks += static_cast<int64_t>(z.second) * n_heads * 16;
+    ++P.n_zero;
   }
   // Longest KV extent first, so that long work items start in the first wave.
-  std::stable_sort(items.begin(), items.end(),
-                   [](const Item& x, const Item& y) { return x.nkv > y.nkv; });
+  std::stable_sort(items.begin(), items.end(), [](const Item& x, const Item& y) {
+    return x.nkv + x.nc > y.nkv + y.nc;
+  });
   int64_t ctas = 0;
   for (size_t i = 0; i < items.size(); ++i) {
     const Item& it = items[i];
     Seg& s = P.seg[i];
     s.q_row0 = it.q0;
     s.nq = it.nq;
-    s.nkv = it.nkv;
+    // A view with no rows is moved second, so that tile 0 always exists.
+    const bool swap = it.nkv == 0;
+    const int kv0 = swap ? it.c0 : it.kv0, nkv = swap ? it.nc : it.nkv;
+    const __nv_bfloat16* k1 = swap ? b.kc : b.k;
+    const __nv_bfloat16* v1 = swap ? b.vc : b.v;
+    const int64_t ks1 = swap ? b.kc_stride : b.k_stride, vs1 = swap ? b.vc_stride : b.v_stride;
+    s.nkv = nkv;
+    s.nkv2 = swap ? 0 : it.nc;
     s.n_pairs = (it.nq + 2 * kBM - 1) / (2 * kBM);
     s.cta0 = static_cast<int32_t>(ctas);
-    ctas += static_cast<int64_t>(s.n_pairs) * a.n_heads;
-    if (!encode_rows(enc, &P.tm_q[i], a.q + static_cast<int64_t>(it.q0) * a.q_stride, a.q_stride,
-                     a.n_heads, it.nq, err) ||
-        !encode_rows(enc, &P.tm_k[i], a.k + static_cast<int64_t>(it.kv0) * a.k_stride, a.k_stride,
-                     a.n_heads, it.nkv, err) ||
-        !encode_rows(enc, &P.tm_v[i], a.v + static_cast<int64_t>(it.kv0) * a.v_stride, a.v_stride,
-                     a.n_heads, it.nkv, err))
+    ctas += static_cast<int64_t>(s.n_pairs) * n_heads;
+    if (!encode_rows(enc, &P.tm_q[i], b.q + static_cast<int64_t>(it.q0) * b.q_stride, b.q_stride,
+                     n_heads, it.nq, err) ||
+        !encode_rows(enc, &P.tm_k[i], k1 + static_cast<int64_t>(kv0) * ks1, ks1, n_heads, nkv,
+                     err) ||
+        !encode_rows(enc, &P.tm_v[i], v1 + static_cast<int64_t>(kv0) * vs1, vs1, n_heads, nkv,
+                     err))
+      return H3_ERR_DEVICE;
+    if (s.nkv2 > 0 &&
+        (!encode_rows(enc, &P.tm_k2[i], b.kc + static_cast<int64_t>(it.c0) * b.kc_stride,
+                      b.kc_stride, n_heads, it.nc, err) ||
+         !encode_rows(enc, &P.tm_v2[i], b.vc + static_cast<int64_t>(it.c0) * b.vc_stride,
+                      b.vc_stride, n_heads, it.nc, err)))
       return H3_ERR_DEVICE;
   }
   if (ctas > 0x7fffffff) {
@@ -580,11 +618,11 @@ int launch_attention(const AttnArgs& a, cudaStream_t stream, std::string& err) {
     return H3_ERR_SHAPE;
   }
   P.n_seg = static_cast<int32_t>(items.size());
-  P.n_heads = a.n_heads;
+  P.n_heads = n_heads;
   P.n_compute_ctas = static_cast<int32_t>(ctas);
-  P.out = a.out;
-  P.out_stride = a.out_stride;
-  P.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+  P.out = b.out;
+  P.out_stride = b.out_stride;
+  P.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   P.epoch = g_epoch_counter.fetch_add(1) + 1;
   P.fault = g_fault_next.exchange(0);
   int64_t grid = ctas;
@@ -612,6 +650,41 @@ int launch_attention(const AttnArgs& a, cudaStream_t stream, std::string& err) {
     return H3_ERR_LAUNCH;
   }
   return H3_OK;
+}
+
+}  // namespace
+
+int launch_attention(const AttnArgs& a, cudaStream_t stream, std::string& err) {
+  std::vector<Item> items;
+  std::vector<std::pair<int, int>> zero;
+  for (int b = 0; b < a.n_seq; ++b) {
+    const int q0 = a.cu_q[b], q_ext = a.cu_q[b + 1] - a.cu_q[b];
+    const int kv0 = a.cu_kv[b], kv_ext = a.cu_kv[b + 1] - a.cu_kv[b];
+    int nq = a.valid ? a.valid[b] : q_ext;
+    const int nkv = a.valid ? a.valid[b] : kv_ext;
+    if (nkv == 0) nq = 0;  // no key: every query row of the segment is 0
+    if (nq > 0) items.push_back({q0, nq, kv0, nkv, 0, 0});
+    if (q_ext > nq) zero.push_back({q0 + nq, q_ext - nq});
+  }
+  const Buffers bufs{a.q, a.k, a.v, nullptr, nullptr, a.out,
+                     a.q_stride, a.k_stride, a.v_stride, 0, 0, a.out_stride};
+  return launch_items(bufs, items, zero, a.n_heads, a.scale, stream, err);
+}
+
+int launch_attention_groups(const AttnGroupArgs& a, cudaStream_t stream, std::string& err) {
+  std::vector<Item> items;
+  std::vector<std::pair<int, int>> zero;
+  for (int g = 0; g < a.n_groups; ++g) {
+    const h3_attn_group& G = a.groups[g];
+    if (G.q_len == 0) continue;
+    if (G.kv_len + G.cache_len == 0)
+      zero.push_back({G.q_start, G.q_len});
+    else
+      items.push_back({G.q_start, G.q_len, G.kv_start, G.kv_len, G.cache_start, G.cache_len});
+  }
+  const Buffers bufs{a.q, a.k, a.v, a.kc, a.vc, a.out,
+                     a.q_stride, a.k_stride, a.v_stride, a.kc_stride, a.vc_stride, a.out_stride};
+  return launch_items(bufs, items, zero, a.n_heads, a.scale, stream, err);
 }
 
 // Device address of the status word on the current device (looked up once

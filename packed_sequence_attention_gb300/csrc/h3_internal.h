@@ -53,6 +53,20 @@ struct AttnArgs {
 // H3_* status and fills `err` on failure.
 int launch_attention(const AttnArgs& a, cudaStream_t stream, std::string& err);
 
+struct AttnGroupArgs {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  const __nv_bfloat16* kc;  // cached K/V (may be null when no group uses them)
+  const __nv_bfloat16* vc;
+  __nv_bfloat16* out;
+  int64_t q_stride, k_stride, v_stride, kc_stride, vc_stride, out_stride;  // elements
+  const h3_attn_group* groups;  // host [n_groups]
+  int n_groups, n_heads;
+  float scale;
+};
+int launch_attention_groups(const AttnGroupArgs& a, cudaStream_t stream, std::string& err);
+
 // Device status word: read (after a device synchronise) and clear.
 cudaError_t read_and_clear_status(uint32_t* out);
 

@@ -252,6 +252,30 @@ def make_inputs(w, seed: Optional[int] = None, fill: str = "A",
     return res
 
 
+def ref_cached_inputs(n_refs: int = 3, seed: int = BASE_SEED + 50, device="cpu") -> dict:
+    """Reference-to-video step after the first (Sol-H3 reference KV caching,
+    Fig. 4): the current sequence holds video 21x24x28 (14,112), audio 1,800
+    and text 510 tokens (16,422 valid of 16,448 rows); the cache holds the
+    K/V of n_refs reference videos of the same latent grid (14,112 rows each)
+    computed in the first step.  Reference query rows are skipped: the
+    16,422 current queries attend to the cache and to the current K/V."""
+    H, D = 42, HEAD_DIM
+    cur_valid, cur_rows, ref_rows = 16422, 16448, 14112 * n_refs
+    gen = torch.Generator(device=torch.device(device)).manual_seed(seed)
+
+    def normal(rows):
+        return torch.randn((rows, H, D), generator=gen, device=device,
+                           dtype=torch.float32).to(torch.bfloat16)
+    q, k, v = normal(cur_rows), normal(cur_rows), normal(cur_rows)
+    kc, vc = normal(ref_rows), normal(ref_rows)
+    for t in (q, k, v):
+        t[cur_valid:] = float("nan")
+    out = torch.full((cur_rows, H, D), float("nan"), dtype=torch.bfloat16, device=device)
+    groups = [(0, cur_valid, 0, cur_valid, 0, ref_rows)]
+    return dict(q=q, k=k, v=v, k_cache=kc, v_cache=vc, out=out, groups=groups, n_heads=H,
+                flops=4.0 * H * D * cur_valid * (cur_valid + ref_rows))
+
+
 def custom(name: str, n_heads: int, segments: Sequence[Segment],
            self_attention: bool = True) -> Workload:
     """A workload for tests: arbitrary heads and segments."""

@@ -123,11 +123,39 @@ def test_attention_rejects_on_host(lib, kw, code):
     assert lib.h3_last_error().decode() != ""
 
 
+def groups_call(lib, groups, **kw):
+    a = dict(q=A, qs=5376, k=A, ks=5376, v=A, vs=5376, kc=A + 0x400000, kcs=5376,
+             vc=A + 0x500000, vcs=5376, o=A + 0x100000, os=5376, n=None, H=42, D=128,
+             scale=0.08838, stream=None)
+    a.update(kw)
+    arr = (_binding.AttnGroup * max(len(groups), 1))(*[_binding.AttnGroup(*g) for g in groups])
+    n = a["n"] if a["n"] is not None else len(groups)
+    return lib.h3_attention_groups(a["q"], a["qs"], a["k"], a["ks"], a["v"], a["vs"], a["kc"],
+                                   a["kcs"], a["vc"], a["vcs"], a["o"], a["os"],
+                                   ctypes.cast(arr, ctypes.c_void_p), n, a["H"], a["D"],
+                                   a["scale"], a["stream"])
+
+
+G_OK = [(0, 100, 0, 100, 0, 50)]
+
+
+@pytest.mark.parametrize("groups,kw,code", [
+    (G_OK, dict(n=0), ARG), (G_OK, dict(n=17), ARG), ([(0, -1, 0, 1, 0, 0)], {}, ARG),
+    ([(0, 10, -5, 1, 0, 0)], {}, ARG), ([(2 ** 31 - 5, 10, 0, 1, 0, 0)], {}, ARG),
+    ([(0, 10, 0, 5, 0, 0), (5, 10, 0, 5, 0, 0)], {}, ARG),          # overlapping query ranges
+    (G_OK, dict(kc=None), ARG), (G_OK, dict(vc=A + 8), ALIGN), (G_OK, dict(kcs=100), SHAPE),
+    (G_OK, dict(D=64), SHAPE), (G_OK, dict(scale=0.0), ARG), (G_OK, dict(os=5380), ALIGN),
+])
+def test_attention_groups_rejects_on_host(lib, groups, kw, code):
+    assert groups_call(lib, groups, **kw) == code
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
 def test_valid_call_without_gpu_reports_device_error(lib):
     assert attn(lib) == DEVICE
     assert norm_rope(lib) == DEVICE
     assert norm_rope_lora(lib) == DEVICE
+    assert groups_call(lib, [(0, 10, 0, 10, 0, 0)], kc=None, vc=None) == DEVICE
     v = ctypes.c_uint32(0)
     assert lib.h3_status_word(ctypes.byref(v)) == DEVICE
 

@@ -387,6 +387,74 @@ def test_attention_row_max_jumps(boost):
     gate(O.widen(out), ref, f"boost {boost}")
 
 
+def _rand(shape, gen):
+    return torch.randn(shape, generator=gen).to(torch.bfloat16)
+
+
+GROUP_CASES = {
+    # name: (heads, q rows, kv rows, cache rows, groups)
+    "ref_cache": (3, 300, 300, 500, [(0, 260, 0, 260, 0, 500)]),
+    "overlapping_views": (2, 200, 400, 0, [(0, 50, 0, 300, 0, 0), (50, 130, 100, 300, 0, 0),
+                                          (180, 20, 399, 1, 0, 0)]),
+    "cache_only_and_empty": (2, 160, 64, 333, [(0, 40, 0, 0, 17, 300), (40, 60, 0, 0, 0, 0),
+                                             (100, 50, 10, 54, 1, 129)]),
+    "skipped_rows": (2, 400, 400, 256, [(100, 150, 0, 400, 0, 256), (300, 77, 300, 100, 128, 128)]),
+}
+
+
+@pytest.mark.parametrize("case", sorted(GROUP_CASES))
+def test_attention_groups_cases(case):
+    H, nq, nkv, nc, groups = GROUP_CASES[case]
+    gen = torch.Generator().manual_seed(zlib.crc32(case.encode()))
+    q, k, v = _rand((nq, H, 128), gen), _rand((nkv, H, 128), gen), _rand((nkv, H, 128), gen)
+    kc = _rand((max(nc, 1), H, 128), gen)
+    vc = _rand((max(nc, 1), H, 128), gen)
+    out = torch.full((nq, H, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    h3.attention_groups(q.cuda(), k.cuda(), v.cuda(), groups, kc.cuda(), vc.cuda(), SCALE, out=out)
+    torch.cuda.synchronize()
+    rows, ref = O.attention_groups(O.widen(q), O.widen(k), O.widen(v), O.widen(kc), O.widen(vc),
+                                   groups, SCALE)
+    got = O.widen(out)
+    if np.linalg.norm(ref) > 0:
+        gate(got[rows], ref, case)
+    assert (got[rows][np.linalg.norm(ref.reshape(len(rows), -1), axis=1) == 0] == 0).all()
+    untouched = np.setdiff1d(np.arange(nq), rows)
+    assert np.isnan(got[untouched]).all(), "rows outside every group must not be written"
+
+
+def test_attention_groups_equal_cu_seqlens_bitwise():
+    g = to_dev(W.make_inputs("stage1_batch2"))
+    run_prologue(g)
+    a = run_attention(g).clone()
+    groups = [(0, 16422, 0, 16422, 0, 0), (16448, 16422, 16448, 16422, 0, 0)]
+    b = torch.full_like(a, float("nan"))
+    h3.attention_groups(g["q"], g["k"], g["v"], groups, scale=SCALE, out=b)
+    torch.cuda.synchronize()
+    for r0 in (0, 16448):
+        assert torch.equal(a[r0:r0 + 16422].view(torch.int16), b[r0:r0 + 16422].view(torch.int16))
+
+
+def test_attention_groups_ref_cached_full_size_sampled():
+    inp = W.ref_cached_inputs(device="cuda")
+    out = h3.attention_groups(inp["q"], inp["k"], inp["v"], inp["groups"], inp["k_cache"],
+                              inp["v_cache"], SCALE, out=inp["out"])
+    torch.cuda.synchronize()
+    n, nc = 16422, inp["k_cache"].shape[0]
+    rows = sample_rows(W.Segment(16448, 16448, n, (21, 24, 28), 1800, 510), 0)
+    rows_t = torch.as_tensor(rows)
+    qc, kc, vc = inp["q"].cpu(), inp["k"].cpu(), inp["v"].cpu()
+    kcc, vcc = inp["k_cache"].cpu(), inp["v_cache"].cpu()
+    got = O.widen(out.cpu()[rows_t])
+    ref = np.zeros_like(got)
+    for h in range(42):
+        _, r = O.attention_groups(O.widen(qc[rows_t, h:h + 1]), O.widen(kc[:n, h:h + 1]),
+                                  O.widen(vc[:n, h:h + 1]), O.widen(kcc[:, h:h + 1]),
+                                  O.widen(vcc[:, h:h + 1]), [(0, len(rows), 0, n, 0, nc)], SCALE)
+        ref[:, h] = r[:, 0]
+    gate(got, ref, "ref-cached full size")
+    assert torch.isnan(out[n:].float()).all()  # padded rows belong to no group
+
+
 def test_closed_forms_on_gpu():
     # all V rows equal -> out = that row; single valid key -> out = v_0
     H, L = 2, 300

@@ -231,6 +231,41 @@ def pin_attention_invariants(Ox):
     return worst
 
 
+def pin_attention_groups(Ox):
+    """Groups over KV views: (i) disjoint views without a cache reproduce
+    ``attention`` over cu_seqlens; (ii) splitting a view between the current
+    and the cache tensors changes nothing; (iii) key order is irrelevant;
+    (iv) torch SDPA in float64 on the concatenated keys; (v) a group with no
+    key outputs zeros."""
+    rng = np.random.default_rng(10)
+    H, D = 2, 128
+    q = rng.standard_normal((60, H, D)); k = rng.standard_normal((90, H, D))
+    v = rng.standard_normal((90, H, D))
+    kc = rng.standard_normal((40, H, D)); vc = rng.standard_normal((40, H, D))
+    groups = [(0, 20, 0, 30, 0, 0), (20, 40, 30, 60, 0, 0)]
+    rows, got = Ox.attention_groups(q, k, v, kc, vc, groups, 0.2)
+    ref = Ox.attention(q, k, v, [0, 20, 60], [0, 30, 90], None, 0.2)
+    worst = float(np.max(np.abs(got - ref[rows])))
+    # (ii) keys 50..89 moved to the cache tensors
+    kc2 = np.concatenate([k[50:90], kc]); vc2 = np.concatenate([v[50:90], vc])
+    rows2, got2 = Ox.attention_groups(q, k, v, kc2, vc2, [(20, 40, 30, 20, 0, 40)], 0.2)
+    worst = max(worst, float(np.max(np.abs(got2 - got[20:]))))
+    # (iii) + (iv) overlapping views with a cache range against SDPA
+    g = [(5, 30, 10, 50, 7, 33), (30, 25, 0, 70, 0, 0)]
+    rows3, got3 = Ox.attention_groups(q, k, v, kc, vc, g, 0.15)
+    for (q0, nq, k0, nk, c0, nc), lo in zip(g, (0, 30)):
+        kk = np.concatenate([kc[c0:c0 + nc], k[k0:k0 + nk]])   # other key order
+        vv = np.concatenate([vc[c0:c0 + nc], v[k0:k0 + nk]])
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a.transpose(1, 0, 2)))[None]
+        sd = torch.nn.functional.scaled_dot_product_attention(
+            t(q[q0:q0 + nq]), t(kk), t(vv), scale=0.15)[0].numpy().transpose(1, 0, 2)
+        worst = max(worst, float(np.max(np.abs(got3[lo:lo + nq] - sd))))
+    # (v) no key
+    rows4, got4 = Ox.attention_groups(q, k, v, kc, vc, [(0, 4, 0, 0, 0, 0)], 0.2)
+    worst = max(worst, float(np.max(np.abs(got4))), 0.0 if list(rows4) == [0, 1, 2, 3] else 1.0)
+    return worst
+
+
 def pin_softmax_rows(Ox):
     rng = np.random.default_rng(7)
     s = rng.standard_normal((9, 300)) * 40.0
@@ -288,6 +323,7 @@ PINS = [
     (pin_attention_invariants, 1e-12),
     (pin_softmax_rows, 1e-9),
     (pin_round_bf16, 0.0),
+    (pin_attention_groups, 1e-12),
     (pin_lora_prologue, 1e-12),
 ]
 
@@ -405,6 +441,10 @@ def _round_half_up(x):
     return np.floor(x / q + 0.5) * q
 
 
+def _groups_ignore_cache(q, k, v, kc, vc, groups, scale, rows=None):
+    return O.attention_groups(q, k, v, kc, vc, [g[:4] + (0, 0) for g in groups], scale, rows)
+
+
 def _lora_no_round(base, delta, w, pos, sections=SECTIONS, theta=THETA, eps=EPS):
     return O.qk_norm_rope(base + delta, w, pos, sections, theta, eps)
 
@@ -424,6 +464,7 @@ MUTANTS = {
     "round_truncates": dict(round_bf16=_round_trunc),
     "round_half_up": dict(round_bf16=_round_half_up),
     "lora_skips_rounding": dict(qk_norm_rope_lora=_lora_no_round),
+    "groups_ignore_cache": dict(attention_groups=_groups_ignore_cache),
 }
 
 
