@@ -218,6 +218,68 @@ def attention_groups(q: np.ndarray, k: np.ndarray, v: np.ndarray,
     return np.concatenate(sel_rows), np.concatenate(outs, axis=0)
 
 
+# ------------------------------------------------- block-sparse attention
+# Sol-Attn as Sol-H3 (arXiv 2609.35110) section 3.4 describes it: for each
+# query block the threshold is mu + tau * sigma over that block's block-level
+# scores against all KV blocks; KV blocks scoring above it are attended.
+# "Safety rails and the exact prefix KV sink": queries of the prefix
+# [text | conditioning video | audio] attend densely; the prefix KV blocks
+# are always attended by the remaining (target-video) queries.
+# Readings (the page leaves them open): the block-level score of query block
+# a and KV block b is scale * <mean of the block's queries, mean of the
+# block's keys>; sigma is the population standard deviation; "exceed" is a
+# strict >; a block that contains any prefix row counts as a prefix block.
+
+def block_means(x: np.ndarray, n_rows: int, block: int) -> np.ndarray:
+    """x [rows, H, D] -> [ceil(n_rows / block), H, D]: mean over each block's
+    rows among the first n_rows (the last block may be partial)."""
+    nb = -(-n_rows // block)
+    out = np.zeros((nb, x.shape[1], x.shape[2]))
+    for b in range(nb):
+        out[b] = x[b * block:min(n_rows, (b + 1) * block)].mean(axis=0)
+    return out
+
+
+def block_scores(q_means: np.ndarray, k_means: np.ndarray, scale: float) -> np.ndarray:
+    """[nQB, H, D] x [nKB, H, D] -> [H, nQB, nKB] = scale * q_mean . k_mean."""
+    return scale * np.einsum("ahd,bhd->hab", q_means, k_means)
+
+
+def select_blocks(scores: np.ndarray, tau: float, n_prefix_blocks: int) -> np.ndarray:
+    """bool [H, nQB, nKB]: the KV blocks each query block attends.
+
+    Query blocks a < n_prefix_blocks attend to every KV block; otherwise KV
+    block b is kept when b < n_prefix_blocks (sink) or its score exceeds
+    mean + tau * std of the row (population std over all KV blocks)."""
+    mu = scores.mean(axis=-1, keepdims=True)
+    sd = scores.std(axis=-1, keepdims=True)
+    keep = scores > mu + tau * sd
+    keep[:, :, :n_prefix_blocks] = True
+    keep[:, :n_prefix_blocks, :] = True
+    return keep
+
+
+def block_sparse_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, n_rows: int,
+                           keep: np.ndarray, block: int, scale: float, rows=None) -> np.ndarray:
+    """Exact softmax attention of each query row over the keys of the KV
+    blocks its query block keeps (rows past n_rows are padding: output 0)."""
+    H, D = q.shape[1], q.shape[2]
+    if rows is None:
+        rows = np.arange(q.shape[0])
+    rows = np.asarray(rows)
+    out = np.zeros((rows.size, H, D))
+    for i, r in enumerate(rows):
+        if r >= n_rows:
+            continue
+        a = r // block
+        for h in range(H):
+            kb = np.nonzero(keep[h, a])[0]
+            cols = np.concatenate([np.arange(b * block, min(n_rows, (b + 1) * block)) for b in kb])
+            s = scale * (k[cols, h] @ q[r, h])
+            out[i, h] = softmax_rows(s[None])[0] @ v[cols, h]
+    return out
+
+
 def attention_flops(cu_seqlens_q, cu_seqlens_kv, valid_len, n_heads: int,
                     head_dim: int, rows=None) -> float:
     """Valid-token multiply-add count * 2 of the two products (4*H*D*Lq*Lkv),

@@ -266,6 +266,61 @@ def pin_attention_groups(Ox):
     return worst
 
 
+def pin_block_means(Ox):
+    """Rows holding their own index: a full block's mean is b*B + (B-1)/2, the
+    partial last block's mean is the mean of its valid row indices."""
+    B, n = 8, 29
+    x = np.repeat(np.arange(32, dtype=np.float64)[:, None, None], 2, axis=1).repeat(3, axis=2)
+    m = Ox.block_means(x, n, B)
+    exp = np.array([b * B + (B - 1) / 2 for b in range(3)] + [(24 + 28) / 2])
+    return float(np.max(np.abs(m[:, 0, 0] - exp))) + (0.0 if m.shape == (4, 2, 3) else 1.0)
+
+
+def pin_block_selection(Ox):
+    """Hand-worked rows (tau = 0.9): scores (0, 0, 0, 3, 4) have mean 1.4 and
+    population std sqrt(3.04) = 1.7436, threshold 2.969 -> blocks 3 and 4
+    (a sample std would give 3.154 and drop block 3).  A constant row keeps
+    nothing above its mean: only the sinks.  Prefix query blocks keep all."""
+    s = np.array([[[0.0, 0, 0, 3, 4], [2.0, 2, 2, 2, 2], [0.0, 0, 0, 3, 4]]])
+    keep = Ox.select_blocks(s, 0.9, 0)
+    worst = 0.0 if (keep[0, 0].tolist() == [False, False, False, True, True] and
+                    not keep[0, 1].any()) else 1.0
+    keep1 = Ox.select_blocks(s, 0.9, 1)
+    worst += 0.0 if (keep1[0, 0].all() and keep1[0, 1].tolist() == [True, False, False, False, False]
+                     and keep1[0, 2].tolist() == [True, False, False, True, True]) else 1.0
+    # larger tau keeps a subset
+    r = np.random.default_rng(11).standard_normal((2, 6, 40))
+    a, b = Ox.select_blocks(r, 1.0, 2), Ox.select_blocks(r, 1.5, 2)
+    worst += 0.0 if (b <= a).all() and a.sum() > b.sum() else 1.0
+    return worst
+
+
+def pin_block_sparse_attention(Ox):
+    """All blocks kept = dense attention; one block kept = SDPA over exactly
+    that block's keys; scores are the scaled dot of the block means."""
+    rng = np.random.default_rng(12)
+    B, n, H = 16, 70, 2
+    q = rng.standard_normal((80, H, 128)); k = rng.standard_normal((80, H, 128))
+    v = rng.standard_normal((80, H, 128))
+    nb = 5
+    keep = np.ones((H, nb, nb), bool)
+    got = Ox.block_sparse_attention(q, k, v, n, keep, B, 0.1)
+    dense = Ox.attention(q, k, v, [0, 80], [0, 80], [n], 0.1)
+    worst = float(np.max(np.abs(got - dense)))
+    keep = np.zeros((H, nb, nb), bool)
+    keep[:, :, 4] = True                       # only the partial last block (rows 64..69)
+    got = Ox.block_sparse_attention(q, k, v, n, keep, B, 0.1)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a.transpose(1, 0, 2)))[None]
+    sd = torch.nn.functional.scaled_dot_product_attention(
+        t(q[:n]), t(k[64:n]), t(v[64:n]), scale=0.1)[0].numpy().transpose(1, 0, 2)
+    worst = max(worst, float(np.max(np.abs(got[:n] - sd))), float(np.max(np.abs(got[n:]))))
+    qm, km = np.zeros((2, 1, 128)), np.zeros((3, 1, 128))
+    qm[0, 0, 0], qm[1, 0, 1], km[2, 0, 0], km[1, 0, 1] = 2.0, 3.0, 5.0, -1.0
+    sc = Ox.block_scores(qm, km, 0.5)
+    exp = np.array([[[0, 0, 5.0], [0, -1.5, 0]]])
+    return max(worst, float(np.max(np.abs(sc - exp))))
+
+
 def pin_softmax_rows(Ox):
     rng = np.random.default_rng(7)
     s = rng.standard_normal((9, 300)) * 40.0
@@ -324,6 +379,9 @@ PINS = [
     (pin_softmax_rows, 1e-9),
     (pin_round_bf16, 0.0),
     (pin_attention_groups, 1e-12),
+    (pin_block_means, 0.0),
+    (pin_block_selection, 0.0),
+    (pin_block_sparse_attention, 1e-12),
     (pin_lora_prologue, 1e-12),
 ]
 
@@ -445,6 +503,32 @@ def _groups_ignore_cache(q, k, v, kc, vc, groups, scale, rows=None):
     return O.attention_groups(q, k, v, kc, vc, [g[:4] + (0, 0) for g in groups], scale, rows)
 
 
+def _select_sample_std(scores, tau, n_prefix):
+    mu = scores.mean(-1, keepdims=True)
+    sd = scores.std(-1, ddof=1, keepdims=True)
+    keep = scores > mu + tau * sd
+    keep[:, :, :n_prefix] = True
+    keep[:, :n_prefix, :] = True
+    return keep
+
+
+def _select_ge(scores, tau, n_prefix):
+    keep = scores >= scores.mean(-1, keepdims=True) + tau * scores.std(-1, keepdims=True)
+    keep[:, :, :n_prefix] = True
+    keep[:, :n_prefix, :] = True
+    return keep
+
+
+def _select_no_sink(scores, tau, n_prefix):
+    keep = scores > scores.mean(-1, keepdims=True) + tau * scores.std(-1, keepdims=True)
+    keep[:, :n_prefix, :] = True
+    return keep
+
+
+def _block_sums(x, n_rows, block):
+    return O.block_means(x, n_rows, block) * block
+
+
 def _lora_no_round(base, delta, w, pos, sections=SECTIONS, theta=THETA, eps=EPS):
     return O.qk_norm_rope(base + delta, w, pos, sections, theta, eps)
 
@@ -465,6 +549,10 @@ MUTANTS = {
     "round_half_up": dict(round_bf16=_round_half_up),
     "lora_skips_rounding": dict(qk_norm_rope_lora=_lora_no_round),
     "groups_ignore_cache": dict(attention_groups=_groups_ignore_cache),
+    "select_sample_std": dict(select_blocks=_select_sample_std),
+    "select_ge": dict(select_blocks=_select_ge),
+    "select_no_sink": dict(select_blocks=_select_no_sink),
+    "block_sums": dict(block_means=_block_sums),
 }
 
 
