@@ -230,6 +230,9 @@ def bench_gpu(args):
     pro_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs])) if w.self_attention else 0.0
     lora = lora_prologue_timing(h3, g, w, stream, pk) if w.self_attention else None
     ref_cached = ref_cached_timing(h3, W, stream, pk) if w.name == "full" else None
+    sol = sol_attention_timing(h3, g, w, stream, pk) if w.name == "full" else None
+    if sol is not None:
+        sol["speedup_vs_dense_attention"] = round(attn_ms / sol["total_ms"], 3)
     status = h3.status_word()
     if status:
         raise SystemExit(f"device status word {status:#x} after the timed region")
@@ -334,7 +337,8 @@ def bench_gpu(args):
         "prologue_alone_us": round(pro_alone_ms * 1e3, 2) if pro_alone_ms else None,
         "prologue_alone_gbs": round(w.prologue_bytes() / (pro_alone_ms * 1e-3) / 1e9, 1)
         if pro_alone_ms else None,
-        "next_rows": {"lora_prologue": lora, "ref_cached_attention": ref_cached},
+        "next_rows": {"lora_prologue": lora, "ref_cached_attention": ref_cached,
+                      "sol_block_sparse": sol},
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 3)},
         "gpu_launches": launches_per_step(w) * args.steps,
@@ -415,6 +419,50 @@ def ref_cached_timing(h3, W, stream, pk, iters=5):
     tf = inp["flops"] / (ms * 1e-3) / 1e12
     return {"ms": round(ms, 3), "tflops": round(tf, 1), "frac_of_burst": round(tf / pk["bf16"], 4),
             "queries": 16422, "keys": 16422 + 42336, "flop": inp["flops"]}
+
+
+def sol_attention_timing(h3, g, w, stream, pk, tau=1.0, iters=5):
+    """Sol-Attn on the 58,758-token sequence read as [text | audio | video]
+    (prefix 2,310 rows = 19 sink blocks): block means of Q and K, selection at
+    tau, then sparse attention.  Reports the kept fraction of (query block,
+    KV block) pairs, stage times, and TFLOP/s over the kept pairs."""
+    s = w.segments[0]
+    n = s.n_valid_q()
+    q, k, v = g["q"], g["k"], g["v"]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+
+    def run(record):
+        if record:
+            ev[0].record(stream)
+        qm = h3.block_means(q, n)
+        km = h3.block_means(k, n)
+        if record:
+            ev[1].record(stream)
+        lists, counts = h3.block_select(qm, km, tau, -(-2310 // 128), SCALE)
+        if record:
+            ev[2].record(stream)
+        h3.sparse_attention(q, k, v, lists, counts, n, SCALE, out=g["out"])
+        if record:
+            ev[3].record(stream)
+        return counts
+
+    counts = run(False)
+    torch.cuda.synchronize()
+    t = np.zeros(3)
+    for _ in range(iters):
+        run(True)
+        torch.cuda.synchronize()
+        t += [ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2]), ev[2].elapsed_time(ev[3])]
+    t /= iters
+    nb = -(-n // 128)
+    kept = float(counts.double().sum().item()) / (w.n_heads * nb * nb)
+    flops_kept = kept * w.attention_flops()
+    total_ms = float(t.sum())
+    return {"tau": tau, "kept_fraction": round(kept, 4), "means_ms": round(t[0], 3),
+            "select_ms": round(t[1], 3), "attention_ms": round(t[2], 3),
+            "total_ms": round(total_ms, 3),
+            "tflops_over_kept": round(flops_kept / (t[2] * 1e-3) / 1e12, 1),
+            "speedup_vs_dense_attention": None}
 
 
 def committed_traffic(w):

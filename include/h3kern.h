@@ -195,6 +195,52 @@ int h3_attention_groups(const void* q, int64_t q_row_stride, const void* k, int6
                         const h3_attn_group* groups, int n_groups, int n_heads, int head_dim,
                         float scale, h3_stream_t stream);
 
+/*
+ * Sol-Attn block-sparse attention (Sol-H3, section 3.4 "Per-step dynamic
+ * sparsity" and "Safety rails and the exact prefix KV sink"), in three
+ * stages over one packed sequence of n_rows rows, blocks of 128 rows
+ * (n_b = ceil(n_rows / 128) <= 2048, the last block may be partial):
+ *
+ *   h3_block_means    q_means, k_means = per-block mean rows of Q and K;
+ *   h3_block_select   per head and query block a, score(a, b) =
+ *                     scale * <q_means[a], k_means[b]>; KV block b is kept when
+ *                     score > mean_b(score) + tau * std_b(score) (population
+ *                     std), or b < n_prefix_blocks (prefix sink), or
+ *                     a < n_prefix_blocks (prefix queries are dense);
+ *   h3_sparse_attention  exact softmax attention of each query row over the
+ *                     keys of the blocks its query block keeps.
+ *
+ * The pages leave "block-level score" undefined; the block-mean dot product
+ * above is the reading taken.  A block holding any prefix row counts as a
+ * prefix block (n_prefix_blocks = ceil(prefix rows / 128)).
+ */
+
+/* x: device bf16 [n_rows, n_heads, 128] (row stride in elements, 16-byte
+ * aligned); means: device fp32 [n_b, n_heads, 128], 4-byte aligned. */
+int h3_block_means(const void* x, int64_t row_stride, int64_t n_rows, int n_heads, int head_dim,
+                   float* means, h3_stream_t stream);
+
+/* q_means [n_q_blocks, n_heads, 128], k_means [n_kv_blocks, n_heads, 128]
+ * (device fp32, 16-byte aligned; n_kv_blocks <= 2048).  Outputs (device,
+ * 4-byte aligned): lists int32 [n_heads, n_q_blocks, n_kv_blocks], row (h, a)
+ * holding the kept KV blocks in ascending order in its first counts[h, a]
+ * entries; counts int32 [n_heads, n_q_blocks]; scores fp32 [n_heads,
+ * n_q_blocks, n_kv_blocks] or NULL.  Arithmetic is fp32 in a fixed order
+ * (the selection is deterministic). */
+int h3_block_select(const float* q_means, const float* k_means, int n_q_blocks, int n_kv_blocks,
+                    int n_heads, float scale, float tau, int n_prefix_blocks, float* scores,
+                    int32_t* lists, int32_t* counts, h3_stream_t stream);
+
+/* q, k, v, out: device bf16 [>= n_rows, n_heads, 128] as in h3_attention;
+ * lists / counts as h3_block_select writes them for this sequence
+ * (n_q_blocks = n_kv_blocks = n_b).  Rows of a query block that keeps no
+ * block are written as 0; rows >= n_rows are not written.  List entries
+ * outside [0, n_b) are ignored. */
+int h3_sparse_attention(const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,
+                        const void* v, int64_t v_row_stride, void* out, int64_t out_row_stride,
+                        int64_t n_rows, int n_heads, int head_dim, const int32_t* lists,
+                        const int32_t* counts, float scale, h3_stream_t stream);
+
 /* Message for the last nonzero status returned to the calling thread
  * ("" if none).  The pointer stays valid until the thread's next call. */
 const char* h3_last_error(void);

@@ -262,7 +262,8 @@ def select_blocks(scores: np.ndarray, tau: float, n_prefix_blocks: int) -> np.nd
 def block_sparse_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, n_rows: int,
                            keep: np.ndarray, block: int, scale: float, rows=None) -> np.ndarray:
     """Exact softmax attention of each query row over the keys of the KV
-    blocks its query block keeps (rows past n_rows are padding: output 0)."""
+    blocks its query block keeps (rows past n_rows are padding, and rows of a
+    query block that keeps nothing, output 0)."""
     H, D = q.shape[1], q.shape[2]
     if rows is None:
         rows = np.arange(q.shape[0])
@@ -274,6 +275,8 @@ def block_sparse_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, n_rows: 
         a = r // block
         for h in range(H):
             kb = np.nonzero(keep[h, a])[0]
+            if kb.size == 0:
+                continue  # a query block that keeps no KV block outputs 0
             cols = np.concatenate([np.arange(b * block, min(n_rows, (b + 1) * block)) for b in kb])
             s = scale * (k[cols, h] @ q[r, h])
             out[i, h] = softmax_rows(s[None])[0] @ v[cols, h]

@@ -14,6 +14,9 @@ strides and the current stream:
 * ``attention_groups`` -- query groups over KV views into the current K/V
   plus a cached K/V range (Sol-H3 reference KV caching, Fig. 4; SolarWM
   history K/V reuse).
+* ``block_means`` / ``block_select`` / ``sparse_attention`` (and
+  ``sol_attention`` chaining them) -- Sol-Attn block-sparse attention with
+  the exact prefix KV sink (Sol-H3 section 3.4).
 
 There is no CPU or library fallback: without the built library, or off an
 sm_103 device, every call raises ``H3Error``.
@@ -29,6 +32,7 @@ import torch
 from . import _binding
 
 __all__ = ["H3Error", "qk_norm_rope", "qk_norm_rope_lora", "attention", "attention_groups",
+           "block_means", "block_select", "sparse_attention", "sol_attention",
            "status_word", "lib", "HEAD_DIM", "MAX_SEGMENTS", "attention_block"]
 
 HEAD_DIM = 128
@@ -184,6 +188,74 @@ def attention_groups(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, groups,
         out.data_ptr(), strides["out"], ctypes.cast(arr, ctypes.c_void_p), len(groups), H,
         HEAD_DIM, float(scale), _stream(stream)))
     return out
+
+
+BLOCK = 128  # block-sparse blocks = attention tiles
+
+
+def block_means(x: torch.Tensor, n_rows: Optional[int] = None, stream=None) -> torch.Tensor:
+    """fp32 [ceil(n_rows / 128), H, 128]: mean of each 128-row block."""
+    xs = _row_stride(x, "x")
+    n_rows = x.shape[0] if n_rows is None else n_rows
+    H = x.shape[1]
+    out = torch.empty((-(-n_rows // BLOCK), H, HEAD_DIM), dtype=torch.float32, device=x.device)
+    _check(lib().h3_block_means(x.data_ptr(), xs, int(n_rows), H, HEAD_DIM, out.data_ptr(),
+                                _stream(stream)))
+    return out
+
+
+def block_select(q_means: torch.Tensor, k_means: torch.Tensor, tau: float, n_prefix_blocks: int,
+                 scale: Optional[float] = None, with_scores: bool = False, stream=None):
+    """(lists int32 [H, nqb, nkb], counts int32 [H, nqb][, scores fp32])."""
+    nqb, H, _ = q_means.shape
+    nkb = k_means.shape[0]
+    for t in (q_means, k_means):
+        if t.dtype != torch.float32 or not t.is_contiguous() or t.shape[1:] != (H, HEAD_DIM):
+            raise ValueError("means must be contiguous fp32 [n_blocks, H, 128]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(HEAD_DIM)
+    dev = q_means.device
+    lists = torch.empty((H, nqb, nkb), dtype=torch.int32, device=dev)
+    counts = torch.empty((H, nqb), dtype=torch.int32, device=dev)
+    scores = torch.empty((H, nqb, nkb), dtype=torch.float32, device=dev) if with_scores else None
+    _check(lib().h3_block_select(q_means.data_ptr(), k_means.data_ptr(), nqb, nkb, H, float(scale),
+                                 float(tau), int(n_prefix_blocks),
+                                 scores.data_ptr() if with_scores else None, lists.data_ptr(),
+                                 counts.data_ptr(), _stream(stream)))
+    return (lists, counts, scores) if with_scores else (lists, counts)
+
+
+def sparse_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, lists: torch.Tensor,
+                     counts: torch.Tensor, n_rows: int, scale: Optional[float] = None,
+                     out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Attention of each query row over the KV blocks its block keeps."""
+    H = q.shape[1]
+    if out is None:
+        out = torch.empty((q.shape[0], H, HEAD_DIM), dtype=torch.bfloat16, device=q.device)
+    strides = [_row_stride(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"))]
+    nb = -(-n_rows // BLOCK)
+    if tuple(lists.shape) != (H, nb, nb) or tuple(counts.shape) != (H, nb) or \
+            lists.dtype != torch.int32 or counts.dtype != torch.int32:
+        raise ValueError("lists / counts do not match the sequence")
+    if n_rows > min(q.shape[0], k.shape[0], v.shape[0], out.shape[0]):
+        raise ValueError("n_rows exceeds the tensors")
+    if scale is None:
+        scale = 1.0 / math.sqrt(HEAD_DIM)
+    _check(lib().h3_sparse_attention(q.data_ptr(), strides[0], k.data_ptr(), strides[1],
+                                     v.data_ptr(), strides[2], out.data_ptr(), strides[3],
+                                     int(n_rows), H, HEAD_DIM, lists.data_ptr(), counts.data_ptr(),
+                                     float(scale), _stream(stream)))
+    return out
+
+
+def sol_attention(q, k, v, n_rows: int, tau: float, n_prefix_rows: int,
+                  scale: Optional[float] = None, out=None, stream=None):
+    """The three block-sparse stages in a row; returns (out, lists, counts)."""
+    qm = block_means(q, n_rows, stream)
+    km = block_means(k, n_rows, stream)
+    lists, counts = block_select(qm, km, tau, -(-n_prefix_rows // BLOCK), scale, stream=stream)
+    out = sparse_attention(q, k, v, lists, counts, n_rows, scale, out, stream)
+    return out, lists, counts
 
 
 def attention_block(q, k, v, wq, wk, pos_thw, cu_seqlens, valid_len,

@@ -37,6 +37,12 @@ SIGNATURES = {
     "h3_attention_groups": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_int64,
                                     c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_int64,
                                     c_void_p, c_int, c_int, c_int, c_float, c_void_p]),
+    "h3_block_means": (c_int, [c_void_p, c_int64, c_int64, c_int, c_int, c_void_p, c_void_p]),
+    "h3_block_select": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_float, c_float, c_int,
+                                c_void_p, c_void_p, c_void_p, c_void_p]),
+    "h3_sparse_attention": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_int64,
+                                    c_void_p, c_int64, c_int64, c_int, c_int, c_void_p, c_void_p,
+                                    c_float, c_void_p]),
     "h3_last_error": (ctypes.c_char_p, []),
     "h3_status_word": (c_int, [c_u32p]),
     "h3_version": (c_int, []),

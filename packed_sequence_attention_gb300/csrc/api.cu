@@ -289,6 +289,94 @@ int h3_attention_groups(const void* q, int64_t q_row_stride, const void* k, int6
   return H3_OK;
 }
 
+int h3_block_means(const void* x, int64_t row_stride, int64_t n_rows, int n_heads, int head_dim,
+                   float* means, h3_stream_t stream) {
+  if (n_rows < 1 || n_rows > int64_t(h3::kMaxSparseBlocks) * 128)
+    return fail(H3_ERR_ARG, "n_rows must be in [1, %d] (got %lld)", h3::kMaxSparseBlocks * 128,
+                (long long)n_rows);
+  if (n_heads < 1 || n_heads > 65535) return fail(H3_ERR_ARG, "n_heads out of range (%d)", n_heads);
+  if (head_dim != h3::kHeadDim) return fail(H3_ERR_SHAPE, "head_dim must be 128 (got %d)", head_dim);
+  if (row_stride < static_cast<int64_t>(n_heads) * h3::kHeadDim)
+    return fail(H3_ERR_SHAPE, "row stride must be >= n_heads*128");
+  if (!x || !means) return fail(H3_ERR_ARG, "null pointer argument");
+  if (!aligned16(x) || (row_stride * 2) % 16) return fail(H3_ERR_ALIGN, "x and its row stride must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(means) & 3u) != 0) return fail(H3_ERR_ALIGN, "means must be 4-byte aligned");
+  int st = check_device();
+  if (st != H3_OK) return st;
+  cudaError_t e = h3::launch_block_means(static_cast<const __nv_bfloat16*>(x), row_stride, n_rows,
+                                         n_heads, means, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(H3_ERR_LAUNCH, "block means launch: %s", cudaGetErrorString(e));
+  return H3_OK;
+}
+
+int h3_block_select(const float* q_means, const float* k_means, int n_q_blocks, int n_kv_blocks,
+                    int n_heads, float scale, float tau, int n_prefix_blocks, float* scores,
+                    int32_t* lists, int32_t* counts, h3_stream_t stream) {
+  if (n_q_blocks < 1 || n_q_blocks > 65535 || n_kv_blocks < 1 || n_kv_blocks > h3::kMaxSparseBlocks)
+    return fail(H3_ERR_ARG, "block counts out of range (%d, %d; at most 65535 and %d)", n_q_blocks,
+                n_kv_blocks, h3::kMaxSparseBlocks);
+  if (n_heads < 1 || n_heads > 65535) return fail(H3_ERR_ARG, "n_heads out of range (%d)", n_heads);
+  if (!std::isfinite(scale) || !std::isfinite(tau)) return fail(H3_ERR_ARG, "scale and tau must be finite");
+  if (n_prefix_blocks < 0 || n_prefix_blocks > n_kv_blocks)
+    return fail(H3_ERR_ARG, "n_prefix_blocks must be in [0, %d]", n_kv_blocks);
+  if (!q_means || !k_means || !lists || !counts) return fail(H3_ERR_ARG, "null pointer argument");
+  if (!aligned16(q_means) || !aligned16(k_means))
+    return fail(H3_ERR_ALIGN, "means must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(lists) & 3u) || (reinterpret_cast<uintptr_t>(counts) & 3u) ||
+      (scores && (reinterpret_cast<uintptr_t>(scores) & 3u)))
+    return fail(H3_ERR_ALIGN, "lists, counts and scores must be 4-byte aligned");
+  int st = check_device();
+  if (st != H3_OK) return st;
+  cudaError_t e = h3::launch_block_select(q_means, k_means, n_q_blocks, n_kv_blocks, n_heads, scale,
+                                          tau, n_prefix_blocks, scores, lists, counts,
+                                          reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(H3_ERR_LAUNCH, "block select launch: %s", cudaGetErrorString(e));
+  return H3_OK;
+}
+
+int h3_sparse_attention(const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,
+                        const void* v, int64_t v_row_stride, void* out, int64_t out_row_stride,
+                        int64_t n_rows, int n_heads, int head_dim, const int32_t* lists,
+                        const int32_t* counts, float scale, h3_stream_t stream) {
+  if (n_rows < 1 || n_rows > int64_t(h3::kMaxSparseBlocks) * 128)
+    return fail(H3_ERR_ARG, "n_rows must be in [1, %d] (got %lld)", h3::kMaxSparseBlocks * 128,
+                (long long)n_rows);
+  if (n_heads < 1) return fail(H3_ERR_ARG, "n_heads must be >= 1 (got %d)", n_heads);
+  if (head_dim != h3::kHeadDim) return fail(H3_ERR_SHAPE, "head_dim must be 128 (got %d)", head_dim);
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return fail(H3_ERR_ARG, "scale must be finite and > 0");
+  const int64_t width = static_cast<int64_t>(n_heads) * h3::kHeadDim;
+  if (q_row_stride < width || k_row_stride < width || v_row_stride < width || out_row_stride < width)
+    return fail(H3_ERR_SHAPE, "row strides must be >= n_heads*128 = %lld", (long long)width);
+  if (!q || !k || !v || !out || !lists || !counts) return fail(H3_ERR_ARG, "null pointer argument");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(H3_ERR_ALIGN, "q, k, v, out must be 16-byte aligned");
+  if ((q_row_stride * 2) % 16 || (k_row_stride * 2) % 16 || (v_row_stride * 2) % 16 ||
+      (out_row_stride * 2) % 16)
+    return fail(H3_ERR_ALIGN, "row strides must be multiples of 8 elements (16 bytes)");
+  if ((reinterpret_cast<uintptr_t>(lists) & 3u) || (reinterpret_cast<uintptr_t>(counts) & 3u))
+    return fail(H3_ERR_ALIGN, "lists and counts must be 4-byte aligned");
+  int st = check_device();
+  if (st != H3_OK) return st;
+  h3::SparseAttnArgs a{};
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k = static_cast<const __nv_bfloat16*>(k);
+  a.v = static_cast<const __nv_bfloat16*>(v);
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.q_stride = q_row_stride;
+  a.k_stride = k_row_stride;
+  a.v_stride = v_row_stride;
+  a.out_stride = out_row_stride;
+  a.n_rows = n_rows;
+  a.n_heads = n_heads;
+  a.lists = lists;
+  a.counts = counts;
+  a.scale = scale;
+  std::string err;
+  st = h3::launch_sparse_attention(a, reinterpret_cast<cudaStream_t>(stream), err);
+  if (st != H3_OK) return fail(st, "%s", err.c_str());
+  return H3_OK;
+}
+
 int h3_status_word(uint32_t* out) {
   if (!out) return fail(H3_ERR_ARG, "out must not be NULL");
   cudaError_t e = h3::read_and_clear_status(out);

@@ -72,8 +72,14 @@ enum {
 };
 constexpr uint32_t kOffTmemSlot = kOffBar + NUM_BARS * 8;
 constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
-constexpr uint32_t kSmemUsed = kOffAbort + 4;
+constexpr uint32_t kOffList = kOffAbort + 4;  // block-sparse mode only
+constexpr uint32_t kListWords = kMaxSparseBlocks / 32;
+constexpr uint32_t kOffListBits = kOffList + 4;                    // [2][kListWords] u32
+constexpr uint32_t kOffListTiles = kOffListBits + 2 * kListWords * 4;  // [kMaxSparseBlocks] u16
+constexpr uint32_t kOffListSel = kOffListTiles + kMaxSparseBlocks * 2;  // [kMaxSparseBlocks] u8
+constexpr uint32_t kSmemUsed = kOffList;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
+constexpr uint32_t kSmemBytesSparse = kOffListSel + kMaxSparseBlocks + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColO = 256;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only if max grows by > 2^8
@@ -107,6 +113,11 @@ struct __align__(128) AttnParams {
   float scale_log2;
   uint32_t epoch;
   int32_t fault;  // test hook: 1 = the producer never loads K/V tile 1
+  // block-sparse mode: per (head, query block) ordered lists of kept KV blocks
+  const int32_t* sp_lists;   // [H, nqb, nkb]
+  const int32_t* sp_counts;  // [H, nqb]
+  int32_t sp_nqb, sp_nkb;
+  int32_t sp_tail;           // valid rows of the last KV block
 };
 
 struct WaitCtx {
@@ -200,6 +211,11 @@ __device__ __forceinline__ void zero_fill(const AttnParams& p) {
   }
 }
 
+// kSparse: Sol-Attn block-sparse mode -- one packed sequence, each query
+// tile attends to the KV tiles its block list keeps; a CTA walks the ordered
+// union of its two tiles' lists and a tile not kept by one query tile
+// contributes P = 0 there.
+template <bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5;
@@ -226,7 +242,55 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   // KV tiles: those of the first view, then those of the second; the online
   // softmax does not depend on the order in which keys are visited.
   const int n_kv1 = (sg.nkv + kBN - 1) / kBN;
-  const int n_kv = n_kv1 + (sg.nkv2 + kBN - 1) / kBN;
+  int n_kv = n_kv1 + (sg.nkv2 + kBN - 1) / kBN;
+  const uint16_t* list_tiles = reinterpret_cast<const uint16_t*>(gbase + kOffListTiles);
+  const uint8_t* list_sel = gbase + kOffListSel;
+  if (kSparse) {
+    // Ordered union of the two query tiles' kept KV blocks (warp 2).
+    if (warp == 2) {
+      uint32_t* bits = reinterpret_cast<uint32_t*>(gbase + kOffListBits);
+      uint16_t* tiles = reinterpret_cast<uint16_t*>(gbase + kOffListTiles);
+      uint8_t* sel = gbase + kOffListSel;
+      const int nwords = (p.sp_nkb + 31) / 32;
+      for (int w = lane; w < 2 * static_cast<int>(kListWords); w += 32) bits[w] = 0u;
+      __syncwarp();
+      for (int t = 0; t < n_tiles; ++t) {
+        const int64_t row = static_cast<int64_t>(head) * p.sp_nqb + (qrow0 / kBM + t);
+        int cnt = p.sp_counts[row];
+        cnt = cnt < 0 ? 0 : (cnt > p.sp_nkb ? p.sp_nkb : cnt);  // lists are not trusted
+        const int32_t* lst = p.sp_lists + row * p.sp_nkb;
+        for (int i = lane; i < cnt; i += 32) {
+          const int b = lst[i];
+          if (b >= 0 && b < p.sp_nkb) atomicOr(&bits[t * kListWords + (b >> 5)], 1u << (b & 31));
+        }
+      }
+      __syncwarp();
+      int base = 0;
+      for (int w0 = 0; w0 < nwords; w0 += 32) {
+        const int w = w0 + lane;
+        const uint32_t b0 = w < nwords ? bits[w] : 0u;
+        const uint32_t b1 = w < nwords ? bits[kListWords + w] : 0u;
+        uint32_t u = b0 | b1;
+        const int n = __popc(u);
+        int incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        int pos = base + incl - n;
+        while (u) {
+          const int bit = __ffs(u) - 1;
+          u &= u - 1;
+          tiles[pos] = static_cast<uint16_t>(w * 32 + bit);
+          sel[pos] = static_cast<uint8_t>(((b0 >> bit) & 1u) | (((b1 >> bit) & 1u) << 1));
+          ++pos;
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) *reinterpret_cast<volatile int*>(gbase + kOffList) = base;
+    }
+  }
 
   // ---- set-up: barriers (thread 0), TMEM (warp 9)
   if (threadIdx.x == 0) {
@@ -254,10 +318,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + kOffTmemSlot);
+  if (kSparse) n_kv = *reinterpret_cast<volatile int*>(gbase + kOffList);
+  // No KV tile at all (block-sparse mode with two empty lists): rows are 0.
+  const bool no_keys = n_kv == 0;
 
   if (warp == 8) {
     // ================================================= TMA producer
-    if (lane == 0 && *abort_flag == 0u) {
+    if (lane == 0 && *abort_flag == 0u && !no_keys) {
       const CUtensorMap* tq = &p.tm_q[si];
       const CUtensorMap* tk1 = &p.tm_k[si];
       const CUtensorMap* tv1 = &p.tm_v[si];
@@ -283,10 +350,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (j >= kNS) ok = wait1(bar(BAR_KVEMPTY + s), (use - 1) & 1, wctx, H3_STATUS_TIMEOUT_LOAD);
         if (!ok) break;
         if (p.fault == 1 && j == 1) continue;  // test hook: leave this stage empty
-        const bool first = j < n_kv1;
+        const bool first = kSparse || j < n_kv1;
         const CUtensorMap* tk = first ? tk1 : tk2;
         const CUtensorMap* tv = first ? tv1 : tv2;
-        const int row = (first ? j : j - n_kv1) * kBN;
+        const int row = (kSparse ? static_cast<int>(list_tiles[j]) : (first ? j : j - n_kv1)) * kBN;
         mbar_arrive_expect_tx(bar(BAR_KFULL + s), kTileBytes);
         for (int h = 0; h < 2; ++h)
           tma_load_3d(sbase + kOffK + s * kTileBytes + h * kHalfBytes, tk, bar(BAR_KFULL + s),
@@ -310,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     __syncwarp();  // lanes 1-31 wait here for lane 0
   } else if (warp == 9) {
     // ================================================= MMA issuer
-    if (lane == 0 && *abort_flag == 0u) {
+    if (lane == 0 && *abort_flag == 0u && !no_keys) {
       // Descriptors are built once; a K step only moves the start address,
       // which is the low field of the descriptor (addresses stay < 256 KB).
       const uint64_t dq0 = sdesc_sw128(sbase + kOffQ, 16, 1024);
@@ -374,7 +441,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   } else {
     // ================================================= softmax (warps 0-7)
     const int t = warp >> 2;
-    if (t < n_tiles && *abort_flag == 0u) {
+    if (t < n_tiles && *abort_flag == 0u && no_keys) {
+      // Block-sparse mode with nothing kept: the tile's valid rows are 0.
+      const int row = qrow0 + t * kBM + (warp & 3) * 32 + lane;
+      if (row < sg.nq) {
+        uint4* dst = reinterpret_cast<uint4*>(
+            p.out + static_cast<int64_t>(sg.q_row0 + row) * p.out_stride + head * kHeadDim);
+        for (int v4 = 0; v4 < 16; ++v4) dst[v4] = make_uint4(0, 0, 0, 0);
+      }
+    } else if (t < n_tiles && *abort_flag == 0u) {
       const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
       const uint32_t tS = tmem + lane_base + kColS + t * 128;
       const uint32_t tO = tmem + lane_base + kColO + t * 128;
@@ -394,7 +469,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, s[q]);
 #pragma unroll
         for (int q = 0; q < 4; ++q) tmem_wait_ld(s[q]);
-        const int kv_tail = (j == n_kv1 - 1) ? tail1 : (j == n_kv - 1) ? tail2 : kBN;
+        if (kSparse && !((list_sel[j] >> t) & 1u)) {
+          // Not kept for this query tile: P = 0, running max and sum unchanged.
+          uint32_t z[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) z[i] = 0u;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) tmem_st16(tS + q * 16, z);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(BAR_PFULL + t));
+          continue;
+        }
+        const int kv_tail = kSparse ? (list_tiles[j] == p.sp_nkb - 1 ? p.sp_tail : kBN)
+                                    : (j == n_kv1 - 1) ? tail1 : (j == n_kv - 1) ? tail2 : kBN;
         if (kv_tail < kBN) {
 #pragma unroll
           for (int q = 0; q < 4; ++q)
@@ -463,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (ok) ok = wait_warp(bar(BAR_OFINAL + t), 0, wctx, H3_STATUS_TIMEOUT_SOFTMAX);
       if (ok) {
         tc_fence_after();
-        const float inv_l = 1.0f / l;
+        const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;  // l == 0: no kept key
         const int row = qrow0 + t * kBM + (warp & 3) * 32 + lane;  // segment-relative
         const bool valid_row = row < sg.nq;
         uint4* dst = reinterpret_cast<uint4*>(
@@ -562,9 +651,15 @@ struct Buffers {
 
 // Work items (at most H3_MAX_SEGMENTS, nq > 0, nkv + nc > 0) and output
 // row ranges to zero -> tensor maps, schedule, one launch.
+struct SparseLists {
+  const int32_t* lists;
+  const int32_t* counts;
+  int nqb, nkb, tail;
+};
+
 int launch_items(const Buffers& b, std::vector<Item>& items,
                  const std::vector<std::pair<int, int>>& zero, int n_heads, float scale,
-                 cudaStream_t stream, std::string& err) {
+                 cudaStream_t stream, std::string& err, const SparseLists* sparse = nullptr) {
   EncodeTiledFn enc = get_encoder(err);
   if (!enc) return H3_ERR_DEVICE;
   thread_local AttnParams P;  // ~11 KB of kernel parameters, rebuilt on every call
@@ -625,25 +720,35 @@ int launch_items(const Buffers& b, std::vector<Item>& items,
   P.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   P.epoch = g_epoch_counter.fetch_add(1) + 1;
   P.fault = g_fault_next.exchange(0);
+  if (sparse != nullptr) {
+    P.sp_lists = sparse->lists;
+    P.sp_counts = sparse->counts;
+    P.sp_nqb = sparse->nqb;
+    P.sp_nkb = sparse->nkb;
+    P.sp_tail = sparse->tail;
+  }
   int64_t grid = ctas;
   if (grid == 0) {
     if (P.zero_chunks == 0) return H3_OK;  // nothing to do
     grid = std::min<int64_t>((P.zero_chunks + 255) / 256, 1024);
   }
 
-  static std::atomic<int> attr_done[64];
+  const bool sp = sparse != nullptr;
+  auto kernel = sp ? attn_fwd_kernel<true> : attn_fwd_kernel<false>;
+  const uint32_t smem = sp ? kSmemBytesSparse : kSmemBytes;
+  static std::atomic<int> attr_done[2][64];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && attr_done[dev].load() == 0) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
+  if (dev >= 0 && dev < 64 && attr_done[sp][dev].load() == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
     if (e != cudaSuccess) {
       err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
       return H3_ERR_DEVICE;
     }
-    attr_done[dev].store(1);
+    attr_done[sp][dev].store(1);
   }
-  attn_fwd_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(P);
+  kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(P);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     err = std::string("attention launch: ") + cudaGetErrorString(e);
@@ -685,6 +790,17 @@ int launch_attention_groups(const AttnGroupArgs& a, cudaStream_t stream, std::st
   const Buffers bufs{a.q, a.k, a.v, a.kc, a.vc, a.out,
                      a.q_stride, a.k_stride, a.v_stride, a.kc_stride, a.vc_stride, a.out_stride};
   return launch_items(bufs, items, zero, a.n_heads, a.scale, stream, err);
+}
+
+int launch_sparse_attention(const SparseAttnArgs& a, cudaStream_t stream, std::string& err) {
+  std::vector<Item> items;
+  std::vector<std::pair<int, int>> zero;
+  items.push_back({0, static_cast<int>(a.n_rows), 0, static_cast<int>(a.n_rows), 0, 0});
+  const Buffers bufs{a.q, a.k, a.v, nullptr, nullptr, a.out,
+                     a.q_stride, a.k_stride, a.v_stride, 0, 0, a.out_stride};
+  const int nb = static_cast<int>((a.n_rows + kBN - 1) / kBN);
+  const SparseLists sl{a.lists, a.counts, nb, nb, static_cast<int>(a.n_rows - (nb - 1) * kBN)};
+  return launch_items(bufs, items, zero, a.n_heads, a.scale, stream, err, &sl);
 }
 
 // Device address of the status word on the current device (looked up once

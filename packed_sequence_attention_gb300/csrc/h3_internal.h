@@ -12,6 +12,9 @@
 namespace h3 {
 
 constexpr int kHeadDim = 128;
+// Block-sparse mode: blocks (and attention tiles) of 128 rows; at most
+// kMaxSparseBlocks blocks per sequence (262,144 rows).
+constexpr int kMaxSparseBlocks = 2048;
 
 // ---------------------------------------------------------------- prologue
 struct NormRopeArgs {
@@ -66,6 +69,26 @@ struct AttnGroupArgs {
   float scale;
 };
 int launch_attention_groups(const AttnGroupArgs& a, cudaStream_t stream, std::string& err);
+
+// ------------------------------------------------------------ block sparse
+cudaError_t launch_block_means(const __nv_bfloat16* x, int64_t stride, int64_t n_rows, int H,
+                               float* out, cudaStream_t stream);
+cudaError_t launch_block_select(const float* qm, const float* km, int nqb, int nkb, int H,
+                                float scale, float tau, int n_prefix, float* scores,
+                                int32_t* lists, int32_t* counts, cudaStream_t stream);
+struct SparseAttnArgs {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  __nv_bfloat16* out;
+  int64_t q_stride, k_stride, v_stride, out_stride;
+  int64_t n_rows;
+  int n_heads;
+  const int32_t* lists;   // device [H, nb, nb]
+  const int32_t* counts;  // device [H, nb]
+  float scale;
+};
+int launch_sparse_attention(const SparseAttnArgs& a, cudaStream_t stream, std::string& err);
 
 // Device status word: read (after a device synchronise) and clear.
 cudaError_t read_and_clear_status(uint32_t* out);

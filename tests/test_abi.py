@@ -150,6 +150,40 @@ def test_attention_groups_rejects_on_host(lib, groups, kw, code):
     assert groups_call(lib, groups, **kw) == code
 
 
+@pytest.mark.parametrize("args,code", [
+    (dict(n=0), ARG), (dict(n=2048 * 128 + 1), ARG), (dict(D=64), SHAPE), (dict(x=None), ARG),
+    (dict(x=A + 8), ALIGN), (dict(m=A + 2), ALIGN), (dict(s=100), SHAPE),
+])
+def test_block_means_rejects_on_host(lib, args, code):
+    a = dict(x=A, s=5376, n=1000, H=42, D=128, m=A)
+    a.update(args)
+    assert lib.h3_block_means(a["x"], a["s"], a["n"], a["H"], a["D"], a["m"], None) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(nkb=2049), ARG), (dict(nqb=0), ARG), (dict(tau=float("inf")), ARG),
+    (dict(npre=9), ARG), (dict(npre=-1), ARG), (dict(lists=None), ARG), (dict(qm=A + 4), ALIGN),
+    (dict(counts=A + 2), ALIGN),
+])
+def test_block_select_rejects_on_host(lib, args, code):
+    a = dict(qm=A, km=A, nqb=8, nkb=8, H=2, scale=0.1, tau=1.0, npre=1, sc=None, lists=A, counts=A)
+    a.update(args)
+    assert lib.h3_block_select(a["qm"], a["km"], a["nqb"], a["nkb"], a["H"], a["scale"], a["tau"],
+                               a["npre"], a["sc"], a["lists"], a["counts"], None) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(n=0), ARG), (dict(D=256), SHAPE), (dict(lists=None), ARG), (dict(q=A + 2), ALIGN),
+    (dict(os_=100), SHAPE), (dict(scale=-1.0), ARG), (dict(counts=A + 1), ALIGN),
+])
+def test_sparse_attention_rejects_on_host(lib, args, code):
+    a = dict(q=A, k=A, v=A, o=A, os_=5376, n=1000, H=42, D=128, lists=A, counts=A, scale=0.1)
+    a.update(args)
+    assert lib.h3_sparse_attention(a["q"], 5376, a["k"], 5376, a["v"], 5376, a["o"], a["os_"],
+                                   a["n"], a["H"], a["D"], a["lists"], a["counts"], a["scale"],
+                                   None) == code
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
 def test_valid_call_without_gpu_reports_device_error(lib):
     assert attn(lib) == DEVICE

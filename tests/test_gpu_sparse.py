@@ -1,0 +1,141 @@
+"""GPU parity of the Sol-Attn block-sparse stages against the fp64 oracle.
+
+Block means and scores are floating point (compared within fp32 error).
+The kept-block lists are integers decided from fp32 scores: they must equal
+the oracle's selection on those same scores except for blocks lying within
+fp32 rounding of the threshold, where either decision is valid.  Sparse
+attention is then compared on the GPU's own lists (the exact mask), and
+must equal the dense kernel bit for bit when every block is kept.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import packed_sequence_attention_gb300 as h3
+from oracle import oracle as O
+from packed_sequence_attention_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+SCALE = 1.0 / math.sqrt(128.0)
+B = 128
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    h3.lib()
+    yield
+    assert h3.status_word() == 0
+
+
+def gate(got, ref, what=""):
+    err = np.abs(got - ref)
+    rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300)
+    assert np.isfinite(got).all() and err.max() <= 2e-2 and rel <= 5e-3, \
+        f"{what}: max_abs={err.max():.3e} rel_l2={rel:.3e}"
+
+
+def inputs(H, rows, seed, structured=False):
+    gen = torch.Generator().manual_seed(seed)
+    q = torch.randn((rows, H, 128), generator=gen)
+    k = torch.randn((rows, H, 128), generator=gen)
+    if structured:  # give blocks distinct directions so selections are not uniform
+        d = torch.randn((-(-rows // B), H, 128), generator=gen)
+        q += 0.8 * d.repeat_interleave(B, 0)[:rows]
+        k += 0.8 * d.repeat_interleave(B, 0)[:rows].roll(3, 0)
+    v = torch.randn((rows, H, 128), generator=gen)
+    return [t.to(torch.bfloat16).cuda() for t in (q, k, v)]
+
+
+def check_lists(lists, counts, scores_gpu, tau, n_prefix):
+    """Lists equal the oracle selection on the GPU's own scores, except for
+    blocks within fp32 rounding of the threshold."""
+    sc = scores_gpu.double().cpu().numpy()
+    keep = O.select_blocks(sc, tau, n_prefix)
+    mu, sd = sc.mean(-1, keepdims=True), sc.std(-1, keepdims=True)
+    margin = np.abs(sc - (mu + tau * sd)) <= 1e-5 * (np.abs(mu) + np.abs(sd) + np.abs(sc)) + 1e-9
+    margin[:, :, :n_prefix] = False
+    margin[:, :n_prefix, :] = False
+    L, C = lists.cpu().numpy(), counts.cpu().numpy()
+    got = np.zeros_like(keep)
+    H, nqb, nkb = keep.shape
+    for h in range(H):
+        for a in range(nqb):
+            row = L[h, a, :C[h, a]]
+            assert (np.diff(row) > 0).all(), "lists must be strictly ascending"
+            got[h, a, row] = True
+    bad = (got != keep) & ~margin
+    assert not bad.any(), f"{int(bad.sum())} selection mismatches away from the threshold"
+    return got
+
+
+@pytest.mark.parametrize("H,rows,tau,prefix", [(3, 1000, 1.0, 130), (2, 2000, 0.5, 0),
+                                               (4, 700, 1.5, 700), (1, 129, 1.0, 1)])
+def test_block_stages_and_sparse_attention(H, rows, tau, prefix):
+    q, k, v = inputs(H, rows, seed=rows + H, structured=True)
+    n_pre = -(-prefix // B)
+    qm, km = h3.block_means(q, rows), h3.block_means(k, rows)
+    lists, counts, scores = h3.block_select(qm, km, tau, n_pre, SCALE, with_scores=True)
+    out = h3.sparse_attention(q, k, v, lists, counts, rows, SCALE)
+    torch.cuda.synchronize()
+    qmr, kmr = O.block_means(O.widen(q), rows, B), O.block_means(O.widen(k), rows, B)
+    assert np.abs(qm.double().cpu().numpy() - qmr).max() <= 1e-5
+    assert np.abs(km.double().cpu().numpy() - kmr).max() <= 1e-5
+    sref = O.block_scores(qm.double().cpu().numpy(), km.double().cpu().numpy(), SCALE)
+    assert np.abs(scores.double().cpu().numpy() - sref).max() <= 1e-5 * max(1.0, np.abs(sref).max())
+    keep = check_lists(lists, counts, scores, tau, n_pre)
+    ref = O.block_sparse_attention(O.widen(q), O.widen(k), O.widen(v), rows, keep, B, SCALE)
+    gate(O.widen(out)[:rows], ref[:rows], f"sparse H={H} rows={rows}")
+
+
+def test_all_blocks_kept_equals_dense_bitwise():
+    g = W.make_inputs("medium", device="cuda")
+    n = 4000
+    qm, km = h3.block_means(g["q"], n), h3.block_means(g["k"], n)
+    lists, counts = h3.block_select(qm, km, -1e30, 0, SCALE)
+    sparse = h3.sparse_attention(g["q"], g["k"], g["v"], lists, counts, n, SCALE)
+    dense = h3.attention(g["q"], g["k"], g["v"], [0, 4096], [0, 4096], [n], SCALE)
+    torch.cuda.synchronize()
+    assert (counts.cpu() == 32).all()
+    assert torch.equal(sparse[:n].view(torch.int16), dense[:n].view(torch.int16))
+
+
+def test_empty_selection_outputs_zero():
+    q, k, v = inputs(2, 384, seed=7)
+    qm = torch.zeros((3, 2, 128), device="cuda")   # constant scores: nothing exceeds the mean
+    km = torch.zeros((3, 2, 128), device="cuda")
+    lists, counts = h3.block_select(qm, km, 0.0, 0, SCALE)
+    out = torch.full((384, 2, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    h3.sparse_attention(q, k, v, lists, counts, 384, SCALE, out=out)
+    torch.cuda.synchronize()
+    assert (counts.cpu() == 0).all() and (out.float() == 0).all()
+
+
+def test_sol_attention_full_size_sampled():
+    # The 58,758-token sequence packed as [text | audio | video] (Sol-H3 3.4
+    # packs the prefix first): prefix = 510 + 1,800 rows -> 19 sink blocks.
+    g = W.make_inputs("full", device="cuda")
+    n, prefix = 58758, 2310
+    out, lists, counts = h3.sol_attention(g["q"], g["k"], g["v"], n, 1.0, prefix, SCALE)
+    torch.cuda.synchronize()
+    nb = -(-n // B)
+    C = counts.cpu().numpy()
+    assert (C[:, :19] == nb).all() and (C >= 19).all() and (C <= nb).all()
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([[0, 2309, 2310, 2431, n - 1], rng.integers(0, n, 40)]))
+    L = lists.cpu().numpy()
+    keep = np.zeros((42, nb, nb), bool)
+    for h in range(42):
+        for a in np.unique(rows // B):
+            keep[h, a, L[h, a, :C[h, a]]] = True
+    qc, kc, vc = g["q"].cpu(), g["k"].cpu(), g["v"].cpu()
+    got = O.widen(out.cpu()[torch.as_tensor(rows)])
+    ref = np.zeros_like(got)
+    for h in range(42):
+        r = O.block_sparse_attention(O.widen(qc[:, h:h + 1]), O.widen(kc[:, h:h + 1]),
+                                     O.widen(vc[:, h:h + 1]), n, keep[h:h + 1], B, SCALE, rows=rows)
+        ref[:, h] = r[:, 0]
+    gate(got, ref, "sol attention full size")
