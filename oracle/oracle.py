@@ -25,6 +25,10 @@ What is computed, with the passage each step follows:
   history K/V reuse).
 * ``qk_norm_rope_lora`` / ``round_bf16`` -- the LoRA consumer fusion of
   Sol-H3 section 3.5 (base + delta rounded to bf16 before the prologue).
+* block-sparse attention (``block_means`` ... ``block_sparse_attention``) --
+  Sol-Attn with the exact prefix KV sink, Sol-H3 section 3.4.
+* wire formats (``pack_qkv``, ``merge_heads``, the INT8 / FP8 records) --
+  Sol-H3 section 3.2, optimized and quantized attention collectives.
 
 Readings taken where the pages are silent (each listed in the design notes):
 RMSNorm per head (128 channels) with weight [H, 128]; eps inside the root;
@@ -281,6 +285,110 @@ def block_sparse_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, n_rows: 
             s = scale * (k[cols, h] @ q[r, h])
             out[i, h] = softmax_rows(s[None])[0] @ v[cols, h]
     return out
+
+
+# ------------------------------------------------------------ wire formats
+# Sol-H3 section 3.2, "Optimized attention collectives" and "Quantized
+# communication": packed QKV goes out destination-major in one pass, the
+# attention output comes back through the inverse head merge, and both may
+# travel in approximate record formats.  Readings (the page fixes the sizes,
+# not every bit): a QKV record is one (token, head) with q, k, v back to
+# back; UE5M3 is unsigned, 5 exponent bits (bias 15) and 3 mantissa bits, all
+# 256 codes finite and positive (value 2^(e-15) * (1 + m/8)); a group of 32
+# values takes the smallest code c with 127 * value(c) >= max |x| and stores
+# rint(x / value(c)) as int8; E4M3 is the OCP FP8 E4M3 format with
+# round-to-nearest-even saturating at +-448.
+
+def pack_qkv(q, k, v, n_dest: int) -> np.ndarray:
+    """[rows, H, D] x3 -> [n_dest, rows, H/n_dest, 3, D]: destination-major,
+    q/k/v of one head back to back."""
+    rows, H, D = q.shape
+    x = np.stack([q, k, v], axis=2)                        # [rows, H, 3, D]
+    return x.reshape(rows, n_dest, H // n_dest, 3, D).transpose(1, 0, 2, 3, 4)
+
+
+def merge_heads(parts: np.ndarray) -> np.ndarray:
+    """[n_src, rows, H/n_src, D] -> [rows, H, D] (source s owns heads
+    s*H/n_src ...)."""
+    n_src, rows, hl, D = parts.shape
+    return parts.transpose(1, 0, 2, 3).reshape(rows, n_src * hl, D)
+
+
+def ue5m3_value(code) -> np.ndarray:
+    code = np.asarray(code, dtype=np.int64)
+    return np.ldexp(1.0 + (code & 7) / 8.0, (code >> 3) - 15)
+
+
+def ue5m3_scale_code(amax) -> np.ndarray:
+    """Smallest code c with 127 * value(c) >= amax (code 255 if none)."""
+    amax = np.asarray(amax, dtype=np.float64)
+    table = 127.0 * ue5m3_value(np.arange(256))
+    return np.minimum(np.searchsorted(table, amax, side="left"), 255)
+
+
+def int8_group32(x: np.ndarray):
+    """x [..., D] -> (int8 values [..., D], uint8 scale codes [..., D/32])."""
+    g = x.reshape(x.shape[:-1] + (x.shape[-1] // 32, 32))
+    codes = ue5m3_scale_code(np.abs(g).max(axis=-1))
+    s = ue5m3_value(codes)[..., None]
+    vals = np.clip(np.rint(g / s), -127, 127).astype(np.int8)
+    return vals.reshape(x.shape), codes.astype(np.uint8)
+
+
+def int8_group32_decode(vals: np.ndarray, codes: np.ndarray) -> np.ndarray:
+    g = vals.astype(np.float64).reshape(vals.shape[:-1] + (vals.shape[-1] // 32, 32))
+    return (g * ue5m3_value(codes)[..., None]).reshape(vals.shape)
+
+
+def e4m3_round(x: np.ndarray) -> np.ndarray:
+    """Nearest E4M3 value (3 mantissa bits, min normal 2^-6, subnormal
+    quantum 2^-9), ties to even, saturated to +-448."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)
+    q = np.ldexp(1.0, np.maximum(e, -5) - 4)   # one unit in the last place
+    r = np.rint(x / q) * q
+    return np.clip(r, -448.0, 448.0)
+
+
+def e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """uint8 E4M3 encoding of values already on the E4M3 grid."""
+    x = np.asarray(x, dtype=np.float64)
+    sign = (np.signbit(x)).astype(np.int64) << 7
+    a = np.abs(x)
+    m, e = np.frexp(a)                        # a = m * 2^e, m in [0.5, 1)
+    normal = a >= 2.0 ** -6
+    exp_field = np.where(normal, e - 1 + 7, 0)
+    frac = np.where(normal, np.rint((a / np.ldexp(1.0, e - 1) - 1.0) * 8), np.rint(a / 2.0 ** -9))
+    frac = np.where(a == 0, 0, frac)
+    return (sign | (exp_field << 3) | frac.astype(np.int64)).astype(np.uint8)
+
+
+def qkv_int8_records(q, k, v) -> np.ndarray:
+    """[rows, H, D] x3 -> uint8 [rows, H, 400]: 3 x 128 int8 values, 12 scale
+    codes (q groups 0-3, k groups, v groups), 4 zero bytes."""
+    rows, H, D = q.shape
+    rec = np.zeros((rows, H, 400), dtype=np.uint8)
+    for t, x in enumerate((q, k, v)):
+        vals, codes = int8_group32(x)
+        rec[..., t * 128:(t + 1) * 128] = vals.view(np.uint8)
+        rec[..., 384 + 4 * t:388 + 4 * t] = codes
+    return rec
+
+
+def out_int8_records(o) -> np.ndarray:
+    """[rows, H, D] -> uint8 [rows, H, 144]: 128 int8 values, 4 scale codes,
+    12 zero bytes (a 16-byte aligned record)."""
+    rows, H, D = o.shape
+    rec = np.zeros((rows, H, 144), dtype=np.uint8)
+    vals, codes = int8_group32(o)
+    rec[..., :128] = vals.view(np.uint8)
+    rec[..., 128:132] = codes
+    return rec
+
+
+def out_fp8_records(o) -> np.ndarray:
+    """[rows, H, D] -> uint8 [rows, H, 128] raw E4M3 bytes, no scale."""
+    return e4m3_bits(e4m3_round(o))
 
 
 def attention_flops(cu_seqlens_q, cu_seqlens_kv, valid_len, n_heads: int,

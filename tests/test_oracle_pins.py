@@ -321,6 +321,75 @@ def pin_block_sparse_attention(Ox):
     return max(worst, float(np.max(np.abs(sc - exp))))
 
 
+def pin_wire_layout(Ox):
+    """Hand-checked element of the destination-major packing, and the head
+    merge inverts it per tensor."""
+    rows, H, D = 2, 4, 3
+    idx = lambda t: np.arange(rows * H * D, dtype=np.float64).reshape(rows, H, D) + 100 * t
+    q, k, v = idx(0), idx(1), idx(2)
+    p = Ox.pack_qkv(q, k, v, 2)                  # [2 dest, 2 rows, 2 heads, 3, D]
+    worst = 0.0 if (p.shape == (2, 2, 2, 3, 3) and p[1, 0, 1, 2, 1] == v[0, 3, 1]
+                    and p[0, 1, 0, 1, 2] == k[1, 0, 2]) else 1.0
+    for t_, x in enumerate((q, k, v)):
+        worst += float(np.max(np.abs(Ox.merge_heads(p[:, :, :, t_, :]) - x)))
+    return worst
+
+
+def pin_ue5m3_int8(Ox):
+    """UE5M3 values by hand; the scale code is the smallest with 127 * s >=
+    amax; int8 group quantisation errs by at most s/2 and a group's largest
+    element lands on |q| >= 112 (consecutive codes differ by <= 1.125x)."""
+    vals = Ox.ue5m3_value(np.array([0, 0x78, 0x79, 0x7F, 0x80, 0xFF]))
+    exp = np.array([2.0 ** -15, 1.0, 1.125, 1.875, 2.0, 2.0 ** 16 * 1.875])
+    worst = float(np.max(np.abs(vals - exp)))
+    amax = np.exp(np.random.default_rng(13).uniform(-9, 14, 2000))
+    c = Ox.ue5m3_scale_code(amax)
+    ok = (127 * Ox.ue5m3_value(c) >= amax) & ((c == 0) | (127 * Ox.ue5m3_value(np.maximum(c - 1, 0)) < amax))
+    worst += 0.0 if ok.all() else 1.0
+    x = np.random.default_rng(14).standard_normal((50, 128)) * 3
+    x[0, :32] = 0.0
+    q, codes = Ox.int8_group32(x)
+    dec = Ox.int8_group32_decode(q, codes)
+    s = np.repeat(Ox.ue5m3_value(codes), 32, axis=-1)
+    worst += float(np.max(np.maximum(np.abs(dec - x) - s / 2, 0)))
+    big = np.abs(q.astype(np.int64)).reshape(50, 4, 32).max(-1)
+    worst += 0.0 if (big[1:] >= 112).all() and (dec[0, :32] == 0).all() else 1.0
+    return worst
+
+
+def pin_e4m3(Ox):
+    """E4M3 by hand (subnormal 2^-9, the 240/248/256 tie, saturation at 448)
+    and against torch's float8_e4m3fn conversion inside its finite range."""
+    x = np.array([2.0 ** -9, 2.0 ** -10, 240.0, 248.0, 464.0, 500.0, -1e6, 1.0])
+    exp = np.array([2.0 ** -9, 0.0, 240.0, 256.0, 448.0, 448.0, -448.0, 1.0])
+    worst = float(np.max(np.abs(Ox.e4m3_round(x) - exp)))
+    bits = Ox.e4m3_bits(Ox.e4m3_round(np.array([2.0 ** -9, 240.0, 256.0, 448.0, -1.0])))
+    worst += 0.0 if list(bits) == [0x01, 0x77, 0x78, 0x7E, 0xB8] else 1.0
+    y = np.random.default_rng(15).standard_normal(20000) * np.exp(np.random.default_rng(16).uniform(-9, 5, 20000))
+    y = torch.from_numpy(y).to(torch.bfloat16).double().numpy()
+    y = y[np.abs(y) <= 464.0]  # torch's cast is finite (saturating) only up to 464
+    ref = torch.from_numpy(y).float().to(torch.float8_e4m3fn)
+    worst += float(np.max(np.abs(Ox.e4m3_round(y) - ref.double().numpy())))
+    worst += 0.0 if np.array_equal(Ox.e4m3_bits(Ox.e4m3_round(y)), ref.view(torch.uint8).numpy()) else 1.0
+    return worst
+
+
+def pin_wire_records(Ox):
+    """Record layouts: value bytes, scale codes and zero padding in place."""
+    rng = np.random.default_rng(17)
+    q, k, v = (rng.standard_normal((3, 2, 128)) for _ in range(3))
+    r = Ox.qkv_int8_records(q, k, v)
+    vals, codes = Ox.int8_group32(k)
+    worst = 0.0 if (r.shape == (3, 2, 400) and (r[..., 396:] == 0).all() and
+                    np.array_equal(r[..., 128:256], vals.view(np.uint8)) and
+                    np.array_equal(r[..., 388:392], codes)) else 1.0
+    o = Ox.out_int8_records(q)
+    worst += 0.0 if o.shape == (3, 2, 144) and (o[..., 132:] == 0).all() else 1.0
+    f = Ox.out_fp8_records(q)
+    worst += 0.0 if f.shape == (3, 2, 128) and f.dtype == np.uint8 else 1.0
+    return worst
+
+
 def pin_softmax_rows(Ox):
     rng = np.random.default_rng(7)
     s = rng.standard_normal((9, 300)) * 40.0
@@ -382,6 +451,10 @@ PINS = [
     (pin_block_means, 0.0),
     (pin_block_selection, 0.0),
     (pin_block_sparse_attention, 1e-12),
+    (pin_wire_layout, 0.0),
+    (pin_ue5m3_int8, 1e-12),
+    (pin_e4m3, 0.0),
+    (pin_wire_records, 0.0),
     (pin_lora_prologue, 1e-12),
 ]
 
@@ -416,6 +489,14 @@ def _mutant(**overrides):
         return ns.qk_norm_rope(ns.round_bf16(base + delta), w, pos, sections, theta, eps)
     if "qk_norm_rope_lora" not in overrides:
         ns.qk_norm_rope_lora = qk_norm_rope_lora
+
+    def int8_group32(x):
+        g = x.reshape(x.shape[:-1] + (x.shape[-1] // 32, 32))
+        codes = ns.ue5m3_scale_code(np.abs(g).max(axis=-1))
+        s = ns.ue5m3_value(codes)[..., None]
+        vals = np.clip(np.rint(g / s), -127, 127).astype(np.int8)
+        return vals.reshape(x.shape), codes.astype(np.uint8)
+    ns.int8_group32 = int8_group32
     ns.attention = attention
     return ns
 
@@ -529,6 +610,24 @@ def _block_sums(x, n_rows, block):
     return O.block_means(x, n_rows, block) * block
 
 
+def _scale_code_down(amax):
+    c = O.ue5m3_scale_code(amax)
+    return np.maximum(c - 1, 0)
+
+
+def _e4m3_no_saturation(x):
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)
+    q = np.ldexp(1.0, np.maximum(e, -5) - 4)
+    return np.rint(x / q) * q
+
+
+def _pack_tensor_major(q, k, v, n_dest):
+    rows, H, D = q.shape
+    x = np.stack([q, k, v], axis=0).reshape(3, rows, n_dest, H // n_dest, D)
+    return x.transpose(2, 1, 3, 0, 4).reshape(n_dest, rows, 3, H // n_dest, D).transpose(0, 1, 3, 2, 4)
+
+
 def _lora_no_round(base, delta, w, pos, sections=SECTIONS, theta=THETA, eps=EPS):
     return O.qk_norm_rope(base + delta, w, pos, sections, theta, eps)
 
@@ -553,6 +652,9 @@ MUTANTS = {
     "select_ge": dict(select_blocks=_select_ge),
     "select_no_sink": dict(select_blocks=_select_no_sink),
     "block_sums": dict(block_means=_block_sums),
+    "scale_code_rounds_down": dict(ue5m3_scale_code=_scale_code_down),
+    "e4m3_no_saturation": dict(e4m3_round=_e4m3_no_saturation),
+    "pack_tensor_major": dict(pack_qkv=_pack_tensor_major),
 }
 
 
