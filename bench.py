@@ -231,6 +231,7 @@ def bench_gpu(args):
     lora = lora_prologue_timing(h3, g, w, stream, pk) if w.self_attention else None
     ref_cached = ref_cached_timing(h3, W, stream, pk) if w.name == "full" else None
     sol = sol_attention_timing(h3, g, w, stream, pk) if w.name == "full" else None
+    wire = wire_timing(h3, g, w, stream, pk) if w.name == "full" else None
     if sol is not None:
         sol["speedup_vs_dense_attention"] = round(attn_ms / sol["total_ms"], 3)
     status = h3.status_word()
@@ -338,7 +339,7 @@ def bench_gpu(args):
         "prologue_alone_gbs": round(w.prologue_bytes() / (pro_alone_ms * 1e-3) / 1e9, 1)
         if pro_alone_ms else None,
         "next_rows": {"lora_prologue": lora, "ref_cached_attention": ref_cached,
-                      "sol_block_sparse": sol},
+                      "sol_block_sparse": sol, "wire_formats": wire},
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 3)},
         "gpu_launches": launches_per_step(w) * args.steps,
@@ -463,6 +464,42 @@ def sol_attention_timing(h3, g, w, stream, pk, tau=1.0, iters=5):
             "total_ms": round(total_ms, 3),
             "tflops_over_kept": round(flops_kept / (t[2] * 1e-3) / 1e12, 1),
             "speedup_vs_dense_attention": None}
+
+
+def wire_timing(h3, g, w, stream, pk, iters=5):
+    """Bandwidth of the attention-boundary wire kernels on the valid rows:
+    packing Q/K/V for 2 destinations (bf16 and block-INT8 records), unpacking
+    one destination's share, and packing the output as FP8 records."""
+    n = w.segments[0].n_valid_q()
+    q, k, v = g["q"][:n], g["k"][:n], g["v"][:n]
+    res = {}
+    elem = n * w.n_heads * 128
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(iters):
+            fn()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        return a0.elapsed_time(a1) / iters * 1e3
+
+    for name, fmt, rec in (("bf16", h3.WIRE_BF16, 768), ("int8", h3.WIRE_INT8, 400)):
+        us = timed(lambda: h3.pack_qkv(q, k, v, 2, fmt))
+        nbytes = 3 * elem * 2 + n * w.n_heads * rec
+        res[f"pack_qkv_{name}"] = {"us": round(us, 1), "gbs": round(nbytes / us / 1e3, 1),
+                                   "frac_hbm_measured": round(nbytes / us / 1e3 / pk["hbm"], 4)}
+    wire8 = h3.pack_qkv(q, k, v, 2, h3.WIRE_INT8)
+    us = timed(lambda: h3.unpack_qkv(wire8[0], h3.WIRE_INT8))
+    nbytes = n * (w.n_heads // 2) * (400 + 3 * 256)
+    res["unpack_qkv_int8"] = {"us": round(us, 1), "gbs": round(nbytes / us / 1e3, 1)}
+    us = timed(lambda: h3.pack_out(g["out"][:n], h3.WIRE_FP8))
+    nbytes = elem * 2 + elem
+    res["pack_out_fp8"] = {"us": round(us, 1), "gbs": round(nbytes / us / 1e3, 1)}
+    del wire8
+    return res
 
 
 def committed_traffic(w):

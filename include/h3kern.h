@@ -241,6 +241,53 @@ int h3_sparse_attention(const void* q, int64_t q_row_stride, const void* k, int6
                         int64_t n_rows, int n_heads, int head_dim, const int32_t* lists,
                         const int32_t* counts, float scale, h3_stream_t stream);
 
+/*
+ * Wire formats at the attention boundary (Sol-H3, section 3.2 "Optimized
+ * attention collectives" and "Quantized communication").  On one GPU there
+ * is no exchange; these calls produce and consume the exchange buffers a
+ * sequence-parallel (Ulysses) all-to-all would move.
+ *
+ *   QKV records, one per (token, head):   H3_WIRE_BF16  768 B  q|k|v bf16
+ *                                          H3_WIRE_INT8  400 B  q|k|v int8 (384 B),
+ *                                                        12 scale codes, 4 zero bytes
+ *   output records, one per (token, head): H3_WIRE_BF16  256 B  bf16
+ *                                          H3_WIRE_INT8  144 B  128 int8, 4 codes, 12 zeros
+ *                                          H3_WIRE_FP8   128 B  E4M3, RNE, saturated +-448
+ * Scale codes are UE5M3 (read as: 5 exponent bits, bias 15, 3 mantissa bits,
+ * every code finite and positive, value = 2^(e-15) * (1 + m/8)), one per 32
+ * channels; a group takes the smallest code with 127 * value >= max|x| and
+ * stores rint(x / value).  INT8 and FP8 are approximate; BF16 records are a
+ * pure permutation (bit-exact).  Wire buffers are device memory, 16-byte
+ * aligned; sizes per record from h3_wire_record_bytes.
+ */
+enum { H3_WIRE_BF16 = 0, H3_WIRE_INT8 = 1, H3_WIRE_FP8 = 2 };
+
+/* Bytes of one record: what = 0 for QKV, 1 for the attention output; -1
+ * for a combination that does not exist (FP8 QKV). */
+int h3_wire_record_bytes(int what, int format);
+
+/* q, k, v [n_rows, n_heads, 128] (own row strides) -> wire
+ * [n_dest][n_rows][n_heads / n_dest] QKV records, destination d holding heads
+ * d * n_heads / n_dest ...; n_dest divides n_heads.  Format BF16 or INT8. */
+int h3_pack_qkv(const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,
+                const void* v, int64_t v_row_stride, int64_t n_rows, int n_heads, int n_dest,
+                int format, void* wire, h3_stream_t stream);
+
+/* wire [n_rows][n_heads_local] QKV records -> q, k, v [n_rows, n_heads_local, 128]
+ * (INT8 values decoded and rounded to bf16). */
+int h3_unpack_qkv(const void* wire, int64_t n_rows, int n_heads_local, int format, void* q,
+                  int64_t q_row_stride, void* k, int64_t k_row_stride, void* v,
+                  int64_t v_row_stride, h3_stream_t stream);
+
+/* out [n_rows, n_heads_local, 128] -> wire [n_rows][n_heads_local] output records. */
+int h3_pack_out(const void* out, int64_t out_row_stride, int64_t n_rows, int n_heads_local,
+                int format, void* wire, h3_stream_t stream);
+
+/* Inverse head merge: wire [n_src][n_rows][n_heads / n_src] output records
+ * -> out [n_rows, n_heads, 128]; n_src divides n_heads. */
+int h3_merge_heads(const void* wire, int64_t n_rows, int n_heads, int n_src, int format, void* out,
+                   int64_t out_row_stride, h3_stream_t stream);
+
 /* Message for the last nonzero status returned to the calling thread
  * ("" if none).  The pointer stays valid until the thread's next call. */
 const char* h3_last_error(void);

@@ -17,6 +17,9 @@ strides and the current stream:
 * ``block_means`` / ``block_select`` / ``sparse_attention`` (and
   ``sol_attention`` chaining them) -- Sol-Attn block-sparse attention with
   the exact prefix KV sink (Sol-H3 section 3.4).
+* ``pack_qkv`` / ``unpack_qkv`` / ``pack_out`` / ``merge_heads`` -- the
+  attention-boundary wire formats: destination-major packed QKV, the inverse
+  head merge, and block-INT8 / FP8 records (Sol-H3 section 3.2).
 
 There is no CPU or library fallback: without the built library, or off an
 sm_103 device, every call raises ``H3Error``.
@@ -33,6 +36,8 @@ from . import _binding
 
 __all__ = ["H3Error", "qk_norm_rope", "qk_norm_rope_lora", "attention", "attention_groups",
            "block_means", "block_select", "sparse_attention", "sol_attention",
+           "WIRE_BF16", "WIRE_INT8", "WIRE_FP8", "wire_record_bytes", "pack_qkv", "unpack_qkv",
+           "pack_out", "merge_heads",
            "status_word", "lib", "HEAD_DIM", "MAX_SEGMENTS", "attention_block"]
 
 HEAD_DIM = 128
@@ -256,6 +261,64 @@ def sol_attention(q, k, v, n_rows: int, tau: float, n_prefix_rows: int,
     lists, counts = block_select(qm, km, tau, -(-n_prefix_rows // BLOCK), scale, stream=stream)
     out = sparse_attention(q, k, v, lists, counts, n_rows, scale, out, stream)
     return out, lists, counts
+
+
+WIRE_BF16, WIRE_INT8, WIRE_FP8 = 0, 1, 2
+
+
+def wire_record_bytes(what: str, fmt: int) -> int:
+    """Bytes of one (token, head) record; what is "qkv" or "out"."""
+    n = lib().h3_wire_record_bytes(0 if what == "qkv" else 1, int(fmt))
+    if n < 0:
+        raise ValueError(f"no {what} record in format {fmt}")
+    return n
+
+
+def pack_qkv(q, k, v, n_dest: int, fmt: int = WIRE_BF16, stream=None) -> torch.Tensor:
+    """uint8 [n_dest, rows, H/n_dest, record]: destination-major packed QKV."""
+    rows, H = q.shape[0], q.shape[1]
+    rec = wire_record_bytes("qkv", fmt)
+    wire = torch.empty((n_dest, rows, H // n_dest, rec), dtype=torch.uint8, device=q.device)
+    s = [_row_stride(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"))]
+    _check(lib().h3_pack_qkv(q.data_ptr(), s[0], k.data_ptr(), s[1], v.data_ptr(), s[2], rows, H,
+                             int(n_dest), int(fmt), wire.data_ptr(), _stream(stream)))
+    return wire
+
+
+def unpack_qkv(wire: torch.Tensor, fmt: int = WIRE_BF16, stream=None):
+    """wire [rows, heads, record] -> (q, k, v) bf16 [rows, heads, 128]."""
+    rows, hl = wire.shape[0], wire.shape[1]
+    if not wire.is_contiguous() or wire.shape[2] != wire_record_bytes("qkv", fmt):
+        raise ValueError("wire must be contiguous [rows, heads, record]")
+    q, k, v = (torch.empty((rows, hl, HEAD_DIM), dtype=torch.bfloat16, device=wire.device)
+               for _ in range(3))
+    _check(lib().h3_unpack_qkv(wire.data_ptr(), rows, hl, int(fmt), q.data_ptr(), hl * HEAD_DIM,
+                               k.data_ptr(), hl * HEAD_DIM, v.data_ptr(), hl * HEAD_DIM,
+                               _stream(stream)))
+    return q, k, v
+
+
+def pack_out(out: torch.Tensor, fmt: int = WIRE_BF16, stream=None) -> torch.Tensor:
+    """uint8 [rows, heads, record]: attention output records."""
+    rows, hl = out.shape[0], out.shape[1]
+    wire = torch.empty((rows, hl, wire_record_bytes("out", fmt)), dtype=torch.uint8,
+                       device=out.device)
+    _check(lib().h3_pack_out(out.data_ptr(), _row_stride(out, "out"), rows, hl, int(fmt),
+                             wire.data_ptr(), _stream(stream)))
+    return wire
+
+
+def merge_heads(wire: torch.Tensor, fmt: int = WIRE_BF16, out=None, stream=None) -> torch.Tensor:
+    """wire [n_src, rows, H/n_src, record] -> out bf16 [rows, H, 128]."""
+    n_src, rows, hl = wire.shape[0], wire.shape[1], wire.shape[2]
+    if not wire.is_contiguous() or wire.shape[3] != wire_record_bytes("out", fmt):
+        raise ValueError("wire must be contiguous [n_src, rows, heads, record]")
+    H = n_src * hl
+    if out is None:
+        out = torch.empty((rows, H, HEAD_DIM), dtype=torch.bfloat16, device=wire.device)
+    _check(lib().h3_merge_heads(wire.data_ptr(), rows, H, n_src, int(fmt), out.data_ptr(),
+                                _row_stride(out, "out"), _stream(stream)))
+    return out
 
 
 def attention_block(q, k, v, wq, wk, pos_thw, cu_seqlens, valid_len,

@@ -43,6 +43,14 @@ SIGNATURES = {
     "h3_sparse_attention": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_int64,
                                     c_void_p, c_int64, c_int64, c_int, c_int, c_void_p, c_void_p,
                                     c_float, c_void_p]),
+    "h3_wire_record_bytes": (c_int, [c_int, c_int]),
+    "h3_pack_qkv": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_int64, c_int64,
+                            c_int, c_int, c_int, c_void_p, c_void_p]),
+    "h3_unpack_qkv": (c_int, [c_void_p, c_int64, c_int, c_int, c_void_p, c_int64, c_void_p,
+                              c_int64, c_void_p, c_int64, c_void_p]),
+    "h3_pack_out": (c_int, [c_void_p, c_int64, c_int64, c_int, c_int, c_void_p, c_void_p]),
+    "h3_merge_heads": (c_int, [c_void_p, c_int64, c_int, c_int, c_int, c_void_p, c_int64,
+                               c_void_p]),
     "h3_last_error": (ctypes.c_char_p, []),
     "h3_status_word": (c_int, [c_u32p]),
     "h3_version": (c_int, []),

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libh3kern.so")
-SOURCES = ["api.cu", "qk_norm_rope.cu", "attention.cu", "block_sparse.cu"]
+SOURCES = ["api.cu", "qk_norm_rope.cu", "attention.cu", "block_sparse.cu", "wire.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "-Xptxas", "-v", "--expt-relaxed-constexpr"]

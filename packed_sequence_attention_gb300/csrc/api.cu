@@ -377,6 +377,151 @@ int h3_sparse_attention(const void* q, int64_t q_row_stride, const void* k, int6
   return H3_OK;
 }
 
+int h3_wire_record_bytes(int what, int format) {
+  if (what == 0) return format == H3_WIRE_BF16 ? 768 : format == H3_WIRE_INT8 ? 400 : -1;
+  if (what == 1)
+    return format == H3_WIRE_BF16 ? 256 : format == H3_WIRE_INT8 ? 144 : format == H3_WIRE_FP8 ? 128 : -1;
+  return -1;
+}
+
+}  // extern "C"
+
+namespace {
+
+int wire_rows_heads(int64_t n_rows, int n_heads, int parts) {
+  if (n_rows < 0 || n_rows > (int64_t(1) << 40)) return fail(H3_ERR_ARG, "n_rows out of range");
+  if (n_heads < 1 || n_heads > 4096) return fail(H3_ERR_ARG, "n_heads out of range (%d)", n_heads);
+  if (parts < 1 || n_heads % parts != 0)
+    return fail(H3_ERR_ARG, "the part count (%d) must divide n_heads (%d)", parts, n_heads);
+  return H3_OK;
+}
+
+int bf16_tensor(const void* p, int64_t stride, int64_t width, const char* name) {
+  if (!p) return fail(H3_ERR_ARG, "%s is NULL", name);
+  if (stride < width) return fail(H3_ERR_SHAPE, "%s row stride must be >= %lld", name, (long long)width);
+  if ((reinterpret_cast<uintptr_t>(p) & 7u) || (stride * 2) % 8)
+    return fail(H3_ERR_ALIGN, "%s and its row stride must be 8-byte aligned", name);
+  return H3_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int h3_pack_qkv(const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,
+                const void* v, int64_t v_row_stride, int64_t n_rows, int n_heads, int n_dest,
+                int format, void* wire, h3_stream_t stream) {
+  int st = wire_rows_heads(n_rows, n_heads, n_dest);
+  if (st != H3_OK) return st;
+  if (format != H3_WIRE_BF16 && format != H3_WIRE_INT8)
+    return fail(H3_ERR_ARG, "QKV wire format must be BF16 or INT8 (got %d)", format);
+  const int64_t w = static_cast<int64_t>(n_heads) * h3::kHeadDim;
+  if ((st = bf16_tensor(q, q_row_stride, w, "q")) || (st = bf16_tensor(k, k_row_stride, w, "k")) ||
+      (st = bf16_tensor(v, v_row_stride, w, "v")))
+    return st;
+  if (!wire) return fail(H3_ERR_ARG, "wire is NULL");
+  if (!aligned16(wire)) return fail(H3_ERR_ALIGN, "wire must be 16-byte aligned");
+  if (n_rows == 0) return H3_OK;
+  if ((st = check_device())) return st;
+  h3::WireQkvArgs a{};
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k = static_cast<const __nv_bfloat16*>(k);
+  a.v = static_cast<const __nv_bfloat16*>(v);
+  a.qs = q_row_stride;
+  a.ks = k_row_stride;
+  a.vs = v_row_stride;
+  a.n_rows = n_rows;
+  a.n_heads = n_heads;
+  a.n_parts = n_dest;
+  a.format = format;
+  a.wire = static_cast<uint8_t*>(wire);
+  cudaError_t e = h3::launch_pack_qkv(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(H3_ERR_LAUNCH, "pack_qkv launch: %s", cudaGetErrorString(e));
+  return H3_OK;
+}
+
+int h3_unpack_qkv(const void* wire, int64_t n_rows, int n_heads_local, int format, void* q,
+                  int64_t q_row_stride, void* k, int64_t k_row_stride, void* v,
+                  int64_t v_row_stride, h3_stream_t stream) {
+  int st = wire_rows_heads(n_rows, n_heads_local, 1);
+  if (st != H3_OK) return st;
+  if (format != H3_WIRE_BF16 && format != H3_WIRE_INT8)
+    return fail(H3_ERR_ARG, "QKV wire format must be BF16 or INT8 (got %d)", format);
+  const int64_t w = static_cast<int64_t>(n_heads_local) * h3::kHeadDim;
+  if ((st = bf16_tensor(q, q_row_stride, w, "q")) || (st = bf16_tensor(k, k_row_stride, w, "k")) ||
+      (st = bf16_tensor(v, v_row_stride, w, "v")))
+    return st;
+  if (!wire) return fail(H3_ERR_ARG, "wire is NULL");
+  if (!aligned16(wire)) return fail(H3_ERR_ALIGN, "wire must be 16-byte aligned");
+  if (n_rows == 0) return H3_OK;
+  if ((st = check_device())) return st;
+  h3::WireQkvArgs a{};
+  a.qm = static_cast<__nv_bfloat16*>(q);
+  a.km = static_cast<__nv_bfloat16*>(k);
+  a.vm = static_cast<__nv_bfloat16*>(v);
+  a.qs = q_row_stride;
+  a.ks = k_row_stride;
+  a.vs = v_row_stride;
+  a.n_rows = n_rows;
+  a.n_heads = n_heads_local;
+  a.n_parts = 1;
+  a.format = format;
+  a.wire = const_cast<uint8_t*>(static_cast<const uint8_t*>(wire));
+  cudaError_t e = h3::launch_unpack_qkv(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(H3_ERR_LAUNCH, "unpack_qkv launch: %s", cudaGetErrorString(e));
+  return H3_OK;
+}
+
+int h3_pack_out(const void* out, int64_t out_row_stride, int64_t n_rows, int n_heads_local,
+                int format, void* wire, h3_stream_t stream) {
+  int st = wire_rows_heads(n_rows, n_heads_local, 1);
+  if (st != H3_OK) return st;
+  if (format != H3_WIRE_BF16 && format != H3_WIRE_INT8 && format != H3_WIRE_FP8)
+    return fail(H3_ERR_ARG, "unknown output wire format %d", format);
+  if ((st = bf16_tensor(out, out_row_stride, static_cast<int64_t>(n_heads_local) * h3::kHeadDim, "out")))
+    return st;
+  if (!wire) return fail(H3_ERR_ARG, "wire is NULL");
+  if (!aligned16(wire)) return fail(H3_ERR_ALIGN, "wire must be 16-byte aligned");
+  if (n_rows == 0) return H3_OK;
+  if ((st = check_device())) return st;
+  h3::WireOutArgs a{};
+  a.out = static_cast<const __nv_bfloat16*>(out);
+  a.os = out_row_stride;
+  a.n_rows = n_rows;
+  a.n_heads = n_heads_local;
+  a.n_parts = 1;
+  a.format = format;
+  a.wire = static_cast<uint8_t*>(wire);
+  cudaError_t e = h3::launch_pack_out(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(H3_ERR_LAUNCH, "pack_out launch: %s", cudaGetErrorString(e));
+  return H3_OK;
+}
+
+int h3_merge_heads(const void* wire, int64_t n_rows, int n_heads, int n_src, int format, void* out,
+                   int64_t out_row_stride, h3_stream_t stream) {
+  int st = wire_rows_heads(n_rows, n_heads, n_src);
+  if (st != H3_OK) return st;
+  if (format != H3_WIRE_BF16 && format != H3_WIRE_INT8 && format != H3_WIRE_FP8)
+    return fail(H3_ERR_ARG, "unknown output wire format %d", format);
+  if ((st = bf16_tensor(out, out_row_stride, static_cast<int64_t>(n_heads) * h3::kHeadDim, "out")))
+    return st;
+  if (!wire) return fail(H3_ERR_ARG, "wire is NULL");
+  if (!aligned16(wire)) return fail(H3_ERR_ALIGN, "wire must be 16-byte aligned");
+  if (n_rows == 0) return H3_OK;
+  if ((st = check_device())) return st;
+  h3::WireOutArgs a{};
+  a.outm = static_cast<__nv_bfloat16*>(out);
+  a.os = out_row_stride;
+  a.n_rows = n_rows;
+  a.n_heads = n_heads;
+  a.n_parts = n_src;
+  a.format = format;
+  a.wire = const_cast<uint8_t*>(static_cast<const uint8_t*>(wire));
+  cudaError_t e = h3::launch_merge_heads(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(H3_ERR_LAUNCH, "merge_heads launch: %s", cudaGetErrorString(e));
+  return H3_OK;
+}
+
 int h3_status_word(uint32_t* out) {
   if (!out) return fail(H3_ERR_ARG, "out must not be NULL");
   cudaError_t e = h3::read_and_clear_status(out);

@@ -90,6 +90,32 @@ struct SparseAttnArgs {
 };
 int launch_sparse_attention(const SparseAttnArgs& a, cudaStream_t stream, std::string& err);
 
+// ------------------------------------------------------------ wire formats
+struct WireQkvArgs {
+  const __nv_bfloat16 *q, *k, *v;  // pack: sources
+  __nv_bfloat16 *qm, *km, *vm;     // unpack: destinations
+  int64_t qs, ks, vs;              // row strides (elements)
+  int64_t n_rows;
+  int n_heads;   // pack: all heads; unpack: heads in the records
+  int n_parts;   // pack: destinations
+  int format;
+  uint8_t* wire;
+};
+struct WireOutArgs {
+  const __nv_bfloat16* out;  // pack: source [rows][n_heads][128]
+  __nv_bfloat16* outm;       // merge: destination [rows][n_heads][128]
+  int64_t os;
+  int64_t n_rows;
+  int n_heads;  // pack: heads in the records; merge: all heads
+  int n_parts;  // merge: sources
+  int format;
+  uint8_t* wire;
+};
+cudaError_t launch_pack_qkv(const WireQkvArgs& a, cudaStream_t s);
+cudaError_t launch_unpack_qkv(const WireQkvArgs& a, cudaStream_t s);
+cudaError_t launch_pack_out(const WireOutArgs& a, cudaStream_t s);
+cudaError_t launch_merge_heads(const WireOutArgs& a, cudaStream_t s);
+
 // Device status word: read (after a device synchronise) and clear.
 cudaError_t read_and_clear_status(uint32_t* out);
 

@@ -184,6 +184,34 @@ def test_sparse_attention_rejects_on_host(lib, args, code):
                                    None) == code
 
 
+def test_wire_record_sizes_on_host(lib):
+    assert [lib.h3_wire_record_bytes(0, f) for f in (0, 1, 2)] == [768, 400, -1]
+    assert [lib.h3_wire_record_bytes(1, f) for f in (0, 1, 2)] == [256, 144, 128]
+    assert lib.h3_wire_record_bytes(2, 0) == -1
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(nd=4), ARG), (dict(nd=0), ARG), (dict(fmt=2), ARG), (dict(q=None), ARG),
+    (dict(q=A + 4), ALIGN), (dict(ks=5375), SHAPE), (dict(wire=A + 8), ALIGN), (dict(H=0), ARG),
+])
+def test_pack_qkv_rejects_on_host(lib, args, code):
+    a = dict(q=A, qs=5376, k=A, ks=5376, v=A, vs=5376, n=10, H=42, nd=2, fmt=1, wire=A)
+    a.update(args)
+    assert lib.h3_pack_qkv(a["q"], a["qs"], a["k"], a["ks"], a["v"], a["vs"], a["n"], a["H"],
+                           a["nd"], a["fmt"], a["wire"], None) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(ns=5), ARG), (dict(fmt=3), ARG), (dict(o=None), ARG), (dict(os_=100), SHAPE),
+    (dict(wire=None), ARG), (dict(wire=A + 4), ALIGN),
+])
+def test_merge_heads_rejects_on_host(lib, args, code):
+    a = dict(wire=A, n=10, H=42, ns=2, fmt=2, o=A, os_=5376)
+    a.update(args)
+    assert lib.h3_merge_heads(a["wire"], a["n"], a["H"], a["ns"], a["fmt"], a["o"], a["os_"],
+                              None) == code
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
 def test_valid_call_without_gpu_reports_device_error(lib):
     assert attn(lib) == DEVICE
