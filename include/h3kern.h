@@ -258,7 +258,11 @@ int h3_sparse_attention(const void* q, int64_t q_row_stride, const void* k, int6
  * channels; a group takes the smallest code with 127 * value >= max|x| and
  * stores rint(x / value).  INT8 and FP8 are approximate; BF16 records are a
  * pure permutation (bit-exact).  Wire buffers are device memory, 16-byte
- * aligned; sizes per record from h3_wire_record_bytes.
+ * aligned; sizes per record from h3_wire_record_bytes.  Tensors are bf16
+ * device memory with 8-byte aligned bases and row strides; n_rows >= 0 and
+ * n_rows * n_heads < 2^31 (more records than device memory holds), else
+ * H3_ERR_ARG; n_rows == 0 launches nothing.
+ * Values are expected finite (a NaN does not raise the group's scale).
  */
 enum { H3_WIRE_BF16 = 0, H3_WIRE_INT8 = 1, H3_WIRE_FP8 = 2 };
 

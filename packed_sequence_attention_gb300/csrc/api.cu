@@ -393,6 +393,8 @@ int wire_rows_heads(int64_t n_rows, int n_heads, int parts) {
   if (n_heads < 1 || n_heads > 4096) return fail(H3_ERR_ARG, "n_heads out of range (%d)", n_heads);
   if (parts < 1 || n_heads % parts != 0)
     return fail(H3_ERR_ARG, "the part count (%d) must divide n_heads (%d)", parts, n_heads);
+  if (n_rows * n_heads >= (int64_t(1) << 31))
+    return fail(H3_ERR_ARG, "n_rows * n_heads must be < 2^31");
   return H3_OK;
 }
 

@@ -22,11 +22,15 @@
 #include <cuda_fp16.h>
 
 #include "h3_internal.h"
+#include "ptx.cuh"
 
 namespace h3 {
 namespace {
 
 constexpr int kWarps = 8;
+using ptx::ffma2;
+using ptx::fadd2;
+using ptx::fmax3;
 
 // value(c) = 2^((c >> 3) - 15) * (1 + (c & 7) / 8), built as fp32 bits
 // (biased exponent (c >> 3) + 112, top 3 mantissa bits c & 7): exact.
@@ -35,22 +39,21 @@ __device__ __forceinline__ float ue5m3_value(int c) {
                          (static_cast<uint32_t>(c & 7) << 20));
 }
 
-// Smallest code c with 127 * value(c) >= amax.  A first guess from the
-// exponent and leading mantissa bits of amax / 127 is corrected with the
-// exact comparison (127 * value has at most 11 significant bits).
+// Smallest code c with 127 * value(c) >= amax.  The code just above
+// fl(amax / 127) is at most one step from the answer (code values are 1/16
+// apart relatively, the two roundings 2^-23), so one exact compare settles
+// it (127 * value has at most 11 significant bits).
 __device__ __forceinline__ int ue5m3_code(float amax) {
-  if (!(amax > 127.0f * ue5m3_value(0))) return 0;
   const uint32_t b = __float_as_uint(amax * (1.0f / 127.0f));
-  int e = static_cast<int>(b >> 23) - 112;
-  int c = e * 8 + static_cast<int>((b >> 20) & 7u) + 1;  // round the mantissa up
-  c = c < 0 ? 0 : (c > 255 ? 255 : c);
-  while (c > 0 && 127.0f * ue5m3_value(c - 1) >= amax) --c;
-  while (c < 255 && 127.0f * ue5m3_value(c) < amax) ++c;
+  int c = (static_cast<int>(b >> 23) - 112) * 8 + static_cast<int>((b >> 20) & 7u) +
+          ((b & 0xFFFFFu) != 0u ? 1 : 0);
+  c = min(max(c, 0), 255);
+  if (c > 0 && 127.0f * ue5m3_value(c - 1) >= amax) --c;
+  else if (c < 255 && 127.0f * ue5m3_value(c) < amax) ++c;
   return c;
 }
 
-__device__ __forceinline__ void load4(const __nv_bfloat16* p, float* f) {
-  const uint2 u = *reinterpret_cast<const uint2*>(p);
+__device__ __forceinline__ void unpack4(uint2 u, float* f) {
   f[0] = __uint_as_float(u.x << 16);
   f[1] = __uint_as_float(u.x & 0xFFFF0000u);
   f[2] = __uint_as_float(u.y << 16);
@@ -63,103 +66,277 @@ __device__ __forceinline__ uint2 pack4_bf16(const float* f) {
   return make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
 }
 
-// Quantise this lane's 4 values of a 32-channel group: returns the 4 int8
-// bytes; *code receives the group's scale code (same in all 8 lanes).
-__device__ __forceinline__ uint32_t quant4(const float* f, int* code) {
-  float a = fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3])));
+__device__ __forceinline__ uint2 ld8(const void* p) {
+  return __ldg(reinterpret_cast<const uint2*>(p));
+}
+
+// rint(x / s), ties to even, for 4 values with |x| <= 127 s, without a
+// division and on the FMA pipe only (paired fp32 operations): the 4 int8
+// results in two's complement, one byte each.  Adding M = 1.5 * 2^23
+// rounds to an integer (ties to even).
+// With r = 1/s correctly rounded, q' = rint(x * r) is within one of the
+// answer and the remainder x - q' s is exact in fp32 (24 bits span it).
+// t = q' + (x - q' s) * r is then within 2^-25 of x / s: an exact tie
+// k + 1/2 comes out as exactly k + 1/2 (the error is below half an ulp),
+// and any other quotient stays more than 2^-6 / 30 away from a half-integer
+// (x has 8 significant bits, s = m 2^b with m in 8..15), so rounding t
+// gives rint(x / s) in every case.  The low byte of t + M is the result.
+__device__ __forceinline__ uint32_t quant4(const float* x, float s, float r) {
+  constexpr float kMagic = 12582912.0f;
+  float q[4], e[4], t[4];
+#pragma unroll
+  for (int i = 0; i < 4; i += 2) {
+    ffma2(q[i], q[i + 1], x[i], x[i + 1], r, r, kMagic, kMagic);
+    fadd2(q[i], q[i + 1], q[i], q[i + 1], -kMagic, -kMagic);      // q' = rint(x r)
+    ffma2(e[i], e[i + 1], q[i], q[i + 1], -s, -s, x[i], x[i + 1]);  // x - q' s, exact
+    ffma2(t[i], t[i + 1], e[i], e[i + 1], r, r, q[i], q[i + 1]);   // q' + (x - q' s) r
+    fadd2(t[i], t[i + 1], t[i], t[i + 1], kMagic, kMagic);
+  }
+  return __byte_perm(__byte_perm(__float_as_uint(t[0]), __float_as_uint(t[1]), 0x0040),
+                     __byte_perm(__float_as_uint(t[2]), __float_as_uint(t[3]), 0x0040), 0x5410);
+}
+
+// max |x| over a 32-channel group (its 8 lanes hold 4 values each).
+__device__ __forceinline__ float group_amax(const float* f) {
+  float a = fmaxf(fmax3(fabsf(f[0]), fabsf(f[1]), fabsf(f[2])), fabsf(f[3]));
   a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
   a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
-  const int c = ue5m3_code(a);
-  *code = c;
-  const float s = ue5m3_value(c);
-  uint32_t out = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    int q = __float2int_rn(__fdiv_rn(f[i], s));
-    q = q > 127 ? 127 : (q < -127 ? -127 : q);
-    out |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * i);
-  }
-  return out;
+  return fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
 }
 
-__device__ __forceinline__ void dequant4(uint32_t bytes, int code, float* f) {
+// Scale codes of N <= 8 items (tensors or records) at once: lane j of each
+// 8-lane group computes the code of item j of that group, then every lane
+// fetches s and 1/s of its group for all items.  Returns this lane's code
+// (item lane & 7, meaningful when that is < N); *sat tells the whole warp
+// whether some group's max lies past 127 s (possible with the largest code
+// only), in which case values must be clamped to +-127 s first.
+template <int N>
+__device__ __forceinline__ int group_scales(const float (&amax)[N], float (&s)[N], float (&r)[N],
+                                            bool* sat) {
+  const int lane = threadIdx.x & 31, j = lane & 7;
+  float a = amax[0];
+#pragma unroll
+  for (int i = 1; i < N; ++i) a = j == i ? amax[i] : a;
+  const int c = ue5m3_code(a);
+  const float sc = ue5m3_value(c), rc = __frcp_rn(sc);
+  *sat = __any_sync(0xffffffffu, j < N && a > 127.0f * sc);
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    s[i] = __shfl_sync(0xffffffffu, sc, (lane & 24) | i);
+    r[i] = __shfl_sync(0xffffffffu, rc, (lane & 24) | i);
+  }
+  return c;
+}
+
+__device__ __forceinline__ void clamp4(float* f, float s) {
+  const float lim = 127.0f * s;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) f[i] = fminf(fmaxf(f[i], -lim), lim);
+}
+
+__device__ __forceinline__ uint2 dequant4(uint32_t bytes, int code) {
   const float s = ue5m3_value(code);
+  float f[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) f[i] = static_cast<float>(static_cast<int8_t>(bytes >> (8 * i))) * s;
+  return pack4_bf16(f);
 }
 
-// Gather the group codes of one tensor (lanes 0, 8, 16, 24 hold groups 0-3)
-// into one little-endian word.
-__device__ __forceinline__ uint32_t gather_codes(int code) {
-  uint32_t w = 0;
+__device__ __forceinline__ uint32_t fp8x4(const float* f) {
+  uint16_t lo, hi;
+  // cvt.rn.satfinite.e4m3x2.f32 d, a, b: a -> upper byte, b -> lower byte
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(f[1]), "f"(f[0]));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(f[3]), "f"(f[2]));
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+__device__ __forceinline__ uint2 fp8x4_to_bf16(uint32_t w) {
+  uint32_t h01, h23;  // e4m3x2 -> f16x2 is exact; f16 -> fp32 -> bf16 is exact too
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"(static_cast<uint16_t>(w & 0xFFFF)));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"(static_cast<uint16_t>(w >> 16)));
+  const __half2 a = *reinterpret_cast<const __half2*>(&h01);
+  const __half2 b = *reinterpret_cast<const __half2*>(&h23);
+  const float f[4] = {__low2float(a), __high2float(a), __low2float(b), __high2float(b)};
+  return pack4_bf16(f);
+}
+
+// Every kernel below: warp w of block b takes the kU consecutive units
+// (row, head) starting at (b * kWarps + w) * kU and issues all their loads
+// before it computes, so a lane has kU loads in flight; lane l owns
+// channels 4l..4l+3 of a head.
+template <int kU>
+struct Units {
+  int64_t r[kU];
+  int h[kU];
+  bool ok[kU];
+  // total < 2^31 (checked on the host), so 32-bit arithmetic suffices.
+  __device__ __forceinline__ Units(int64_t total, int H)
+      : Units(total, H, blockIdx.x * kWarps + (threadIdx.x >> 5)) {}
+  // The kU units of pass p: p * kU, p * kU + 1, ...
+  __device__ __forceinline__ Units(int64_t total, int H, uint32_t pass) {
+    const uint32_t u0 = pass * kU;
+    int64_t row = u0 / static_cast<uint32_t>(H);
+    int head = static_cast<int>(u0 - static_cast<uint32_t>(row) * static_cast<uint32_t>(H));
 #pragma unroll
-  for (int g = 0; g < 4; ++g) w |= static_cast<uint32_t>(__shfl_sync(0xffffffffu, code, 8 * g)) << (8 * g);
-  return w;
-}
+    for (int u = 0; u < kU; ++u) {
+      r[u] = row;
+      h[u] = head;
+      ok[u] = static_cast<int64_t>(u0) + u < total;
+      if (++head == H) {
+        head = 0;
+        ++row;
+      }
+    }
+  }
+};
 
-template <int kFmt>
-__global__ void __launch_bounds__(kWarps * 32) pack_qkv_kernel(
+__global__ void __launch_bounds__(kWarps * 32) pack_qkv_bf16_kernel(
     const __nv_bfloat16* __restrict__ q, int64_t qs, const __nv_bfloat16* __restrict__ k, int64_t ks,
     const __nv_bfloat16* __restrict__ v, int64_t vs, int64_t n_rows, int H, int n_dest,
     uint8_t* __restrict__ wire) {
+  constexpr int kU = 2;
   const int lane = threadIdx.x & 31;
-  const int64_t unit = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-  if (unit >= n_rows * H) return;
-  const int64_t r = unit / H;
-  const int h = static_cast<int>(unit - r * H);
-  const int hl = H / n_dest, d = h / hl, hloc = h - d * hl;
-  const int64_t rec = (static_cast<int64_t>(d) * n_rows + r) * hl + hloc;
-  const __nv_bfloat16* src[3] = {q + r * qs, k + r * ks, v + r * vs};
-  if (kFmt == H3_WIRE_BF16) {
-    uint8_t* dst = wire + rec * 768;
+  const Units<kU> un(n_rows * H, H);
+  const int hl = H / n_dest;
+  uint2 in[kU][3] = {};
 #pragma unroll
-    for (int t = 0; t < 3; ++t)
-      *reinterpret_cast<uint2*>(dst + t * 256 + lane * 8) =
-          *reinterpret_cast<const uint2*>(src[t] + h * kHeadDim + lane * 4);
-  } else {
-    uint8_t* dst = wire + rec * 400;
-    uint32_t codes[3];
-#pragma unroll
-    for (int t = 0; t < 3; ++t) {
-      float f[4];
-      load4(src[t] + h * kHeadDim + lane * 4, f);
-      int code;
-      *reinterpret_cast<uint32_t*>(dst + t * 128 + lane * 4) = quant4(f, &code);
-      codes[t] = gather_codes(code);
+  for (int u = 0; u < kU; ++u) {
+    if (un.ok[u]) {
+      const int64_t c = un.h[u] * kHeadDim + lane * 4;
+      in[u][0] = ld8(q + un.r[u] * qs + c);
+      in[u][1] = ld8(k + un.r[u] * ks + c);
+      in[u][2] = ld8(v + un.r[u] * vs + c);
     }
-    if (lane == 0) *reinterpret_cast<uint4*>(dst + 384) = make_uint4(codes[0], codes[1], codes[2], 0u);
+  }
+#pragma unroll
+  for (int u = 0; u < kU; ++u) {
+    if (!un.ok[u]) break;
+    const int d = un.h[u] / hl, hloc = un.h[u] - d * hl;
+    uint8_t* dst = wire + ((static_cast<int64_t>(d) * n_rows + un.r[u]) * hl + hloc) * 768;
+#pragma unroll
+    for (int t = 0; t < 3; ++t) *reinterpret_cast<uint2*>(dst + t * 256 + lane * 8) = in[u][t];
   }
 }
 
+// Block-INT8 QKV records.  Quantising costs more issue slots than the bytes
+// take to move, so the kernel is persistent and software-pipelined: a warp
+// loads its next pass (kU units) before it quantises the current one.
+constexpr int kInt8PackU = 2;
+
+__global__ void __launch_bounds__(kWarps * 32) pack_qkv_int8_kernel(
+    const __nv_bfloat16* __restrict__ q, int64_t qs, const __nv_bfloat16* __restrict__ k, int64_t ks,
+    const __nv_bfloat16* __restrict__ v, int64_t vs, int64_t n_rows, int H, int n_dest,
+    uint8_t* __restrict__ wire) {
+  constexpr int kU = kInt8PackU;
+  constexpr int kRec = 400;
+  const int lane = threadIdx.x & 31;
+  const int hl = H / n_dest;
+  const int64_t total = n_rows * H;
+  const uint32_t n_pass = static_cast<uint32_t>((total + kU - 1) / kU);
+  const uint32_t stride = gridDim.x * kWarps;
+  auto load = [&](const Units<kU>& un, uint2 (&in)[kU][3]) {
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (un.ok[u]) {
+        const int64_t c = un.h[u] * kHeadDim + lane * 4;
+        in[u][0] = ld8(q + un.r[u] * qs + c);
+        in[u][1] = ld8(k + un.r[u] * ks + c);
+        in[u][2] = ld8(v + un.r[u] * vs + c);
+      }
+    }
+  };
+  uint32_t p = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  Units<kU> un(total, H, p);
+  uint2 in[kU][3] = {};
+  load(un, in);
+  while (p < n_pass) {
+    const uint32_t pn = p + stride;
+    const Units<kU> nx(total, H, pn);
+    uint2 nin[kU][3] = {};
+    load(nx, nin);
+    // items i = 3u + t: unit u, tensor t; scale codes of all 3 kU items at once
+    float f[3 * kU][4], amax[3 * kU], s[3 * kU], rs[3 * kU];
+#pragma unroll
+    for (int i = 0; i < 3 * kU; ++i) {
+      unpack4(in[i / 3][i % 3], f[i]);
+      amax[i] = group_amax(f[i]);
+    }
+    bool sat;
+    const int code = group_scales<3 * kU>(amax, s, rs, &sat);
+    if (sat) {
+#pragma unroll
+      for (int i = 0; i < 3 * kU; ++i) clamp4(f[i], s[i]);
+    }
+    uint8_t* dst[kU];
+    int d = un.h[0] / hl, hloc = un.h[0] - d * hl;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      dst[u] = wire + ((static_cast<int64_t>(d) * n_rows + un.r[u]) * hl + hloc) * kRec;
+      if (++hloc == hl) {
+        hloc = 0;
+        if (++d == n_dest) d = 0;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 3 * kU; ++i)
+      if (un.ok[i / 3])
+        *reinterpret_cast<uint32_t*>(dst[i / 3] + (i % 3) * 128 + lane * 4) = quant4(f[i], s[i], rs[i]);
+    // lane (g, j) holds the code of item j, group g; lane u < kU clears the
+    // pad word of unit u.  Pointers are picked by unrolled compares so that
+    // dst[] stays in registers.
+    const int j = lane & 7, g = lane >> 3;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (!un.ok[u]) break;
+      if (j / 3 == u && j < 3 * kU) dst[u][384 + (j - 3 * u) * 4 + g] = static_cast<uint8_t>(code);
+      if (lane == u) *reinterpret_cast<uint32_t*>(dst[u] + 396) = 0u;
+    }
+    un = nx;
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+#pragma unroll
+      for (int t = 0; t < 3; ++t) in[u][t] = nin[u][t];
+    p = pn;
+  }
+}
+
+// Records of one part are [rows][hl], so unit u is record u.
 template <int kFmt>
 __global__ void __launch_bounds__(kWarps * 32) unpack_qkv_kernel(
     const uint8_t* __restrict__ wire, int64_t n_rows, int hl, __nv_bfloat16* __restrict__ q,
     int64_t qs, __nv_bfloat16* __restrict__ k, int64_t ks, __nv_bfloat16* __restrict__ v,
     int64_t vs) {
+  constexpr int kU = 2;
+  constexpr int kRec = kFmt == H3_WIRE_BF16 ? 768 : 400;
   const int lane = threadIdx.x & 31;
-  const int64_t unit = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-  if (unit >= n_rows * hl) return;
-  const int64_t r = unit / hl;
-  const int h = static_cast<int>(unit - r * hl);
-  __nv_bfloat16* dst[3] = {q + r * qs, k + r * ks, v + r * vs};
-  if (kFmt == H3_WIRE_BF16) {
-    const uint8_t* src = wire + unit * 768;
+  const Units<kU> un(n_rows * hl, hl);
+  uint2 in[kU][3];
+  uint32_t codes[kU][3];
+#pragma unroll
+  for (int u = 0; u < kU; ++u) {
+    if (un.ok[u]) {
+      const uint8_t* src = wire + (un.r[u] * hl + un.h[u]) * kRec;
+      if (kFmt == H3_WIRE_BF16) {
+#pragma unroll
+        for (int t = 0; t < 3; ++t) in[u][t] = ld8(src + t * 256 + lane * 8);
+      } else {
+#pragma unroll
+        for (int t = 0; t < 3; ++t) {
+          in[u][t].x = __ldg(reinterpret_cast<const uint32_t*>(src + t * 128 + lane * 4));
+          codes[u][t] = src[384 + t * 4 + (lane >> 3)];
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kU; ++u) {
+    if (!un.ok[u]) break;
+    const int64_t c = un.h[u] * kHeadDim + lane * 4;
+    __nv_bfloat16* dst[3] = {q + un.r[u] * qs + c, k + un.r[u] * ks + c, v + un.r[u] * vs + c};
 #pragma unroll
     for (int t = 0; t < 3; ++t)
-      *reinterpret_cast<uint2*>(dst[t] + h * kHeadDim + lane * 4) =
-          *reinterpret_cast<const uint2*>(src + t * 256 + lane * 8);
-  } else {
-    const uint8_t* src = wire + unit * 400;
-    const uint4 cw = *reinterpret_cast<const uint4*>(src + 384);
-    const uint32_t cws[3] = {cw.x, cw.y, cw.z};
-#pragma unroll
-    for (int t = 0; t < 3; ++t) {
-      float f[4];
-      dequant4(*reinterpret_cast<const uint32_t*>(src + t * 128 + lane * 4),
-               (cws[t] >> (8 * (lane >> 3))) & 0xFF, f);
-      *reinterpret_cast<uint2*>(dst[t] + h * kHeadDim + lane * 4) = pack4_bf16(f);
-    }
+      *reinterpret_cast<uint2*>(dst[t]) =
+          kFmt == H3_WIRE_BF16 ? in[u][t] : dequant4(in[u][t].x, codes[u][t]);
   }
 }
 
@@ -167,31 +344,57 @@ template <int kFmt>
 __global__ void __launch_bounds__(kWarps * 32) pack_out_kernel(
     const __nv_bfloat16* __restrict__ out, int64_t os, int64_t n_rows, int hl,
     uint8_t* __restrict__ wire) {
+  constexpr int kU = 4;
+  constexpr int kRec = kFmt == H3_WIRE_BF16 ? 256 : (kFmt == H3_WIRE_INT8 ? 144 : 128);
   const int lane = threadIdx.x & 31;
-  const int64_t unit = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-  if (unit >= n_rows * hl) return;
-  const int64_t r = unit / hl;
-  const int h = static_cast<int>(unit - r * hl);
-  const __nv_bfloat16* src = out + r * os + h * kHeadDim + lane * 4;
-  if (kFmt == H3_WIRE_BF16) {
-    *reinterpret_cast<uint2*>(wire + unit * 256 + lane * 8) = *reinterpret_cast<const uint2*>(src);
-  } else if (kFmt == H3_WIRE_INT8) {
-    float f[4];
-    load4(src, f);
-    int code;
-    uint8_t* dst = wire + unit * 144;
-    *reinterpret_cast<uint32_t*>(dst + lane * 4) = quant4(f, &code);
-    const uint32_t c = gather_codes(code);
-    if (lane == 0) *reinterpret_cast<uint4*>(dst + 128) = make_uint4(c, 0u, 0u, 0u);
+  const Units<kU> un(n_rows * hl, hl);
+  uint2 in[kU] = {};
+#pragma unroll
+  for (int u = 0; u < kU; ++u)
+    if (un.ok[u]) in[u] = ld8(out + un.r[u] * os + un.h[u] * kHeadDim + lane * 4);
+  uint8_t* dst[kU];
+#pragma unroll
+  for (int u = 0; u < kU; ++u) dst[u] = wire + (un.r[u] * hl + un.h[u]) * kRec;
+  if constexpr (kFmt == H3_WIRE_INT8) {
+    float f[kU][4], amax[kU], s[kU], rs[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      unpack4(in[u], f[u]);
+      amax[u] = group_amax(f[u]);
+    }
+    bool sat;
+    const int code = group_scales<kU>(amax, s, rs, &sat);
+    if (sat) {
+#pragma unroll
+      for (int u = 0; u < kU; ++u) clamp4(f[u], s[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      if (un.ok[u]) *reinterpret_cast<uint32_t*>(dst[u] + lane * 4) = quant4(f[u], s[u], rs[u]);
+    // lane (g, j) holds the code of record j, group g; lane u < kU clears
+    // the pad bytes of record u
+    const int j = lane & 7, g = lane >> 3;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (!un.ok[u]) break;
+      if (j == u) dst[u][128 + g] = static_cast<uint8_t>(code);
+      if (lane == u) {
+        *reinterpret_cast<uint32_t*>(dst[u] + 132) = 0u;
+        *reinterpret_cast<uint2*>(dst[u] + 136) = make_uint2(0u, 0u);
+      }
+    }
   } else {
-    float f[4];
-    load4(src, f);
-    uint16_t lo, hi;
-    // cvt.rn.satfinite.e4m3x2.f32 d, a, b: a -> upper byte, b -> lower byte
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(f[1]), "f"(f[0]));
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(f[3]), "f"(f[2]));
-    *reinterpret_cast<uint32_t*>(wire + unit * 128 + lane * 4) =
-        static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (!un.ok[u]) break;
+      if (kFmt == H3_WIRE_BF16) {
+        *reinterpret_cast<uint2*>(dst[u] + lane * 8) = in[u];
+      } else {
+        float f[4];
+        unpack4(in[u], f);
+        *reinterpret_cast<uint32_t*>(dst[u] + lane * 4) = fp8x4(f);
+      }
+    }
   }
 }
 
@@ -199,51 +402,75 @@ template <int kFmt>
 __global__ void __launch_bounds__(kWarps * 32) merge_heads_kernel(
     const uint8_t* __restrict__ wire, int64_t n_rows, int H, int n_src,
     __nv_bfloat16* __restrict__ out, int64_t os) {
+  constexpr int kU = 4;
+  constexpr int kRec = kFmt == H3_WIRE_BF16 ? 256 : (kFmt == H3_WIRE_INT8 ? 144 : 128);
   const int lane = threadIdx.x & 31;
-  const int64_t unit = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-  if (unit >= n_rows * H) return;
-  const int64_t r = unit / H;
-  const int h = static_cast<int>(unit - r * H);
-  const int hl = H / n_src, sidx = h / hl, hloc = h - sidx * hl;
-  const int64_t rec = (static_cast<int64_t>(sidx) * n_rows + r) * hl + hloc;
-  __nv_bfloat16* dst = out + r * os + h * kHeadDim + lane * 4;
-  if (kFmt == H3_WIRE_BF16) {
-    *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(wire + rec * 256 + lane * 8);
-  } else if (kFmt == H3_WIRE_INT8) {
-    const uint8_t* src = wire + rec * 144;
-    float f[4];
-    dequant4(*reinterpret_cast<const uint32_t*>(src + lane * 4),
-             src[128 + (lane >> 3)], f);
-    *reinterpret_cast<uint2*>(dst) = pack4_bf16(f);
-  } else {
-    const uint32_t w = *reinterpret_cast<const uint32_t*>(wire + rec * 128 + lane * 4);
-    uint32_t h01, h23;  // e4m3x2 -> f16x2 is exact; f16 -> fp32 -> bf16 is exact too
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"(static_cast<uint16_t>(w & 0xFFFF)));
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"(static_cast<uint16_t>(w >> 16)));
-    const __half2 a = *reinterpret_cast<const __half2*>(&h01);
-    const __half2 b = *reinterpret_cast<const __half2*>(&h23);
-    float f[4] = {__low2float(a), __high2float(a), __low2float(b), __high2float(b)};
-    *reinterpret_cast<uint2*>(dst) = pack4_bf16(f);
+  const Units<kU> un(n_rows * H, H);
+  const int hl = H / n_src;
+  uint2 in[kU];
+  int codes[kU];
+#pragma unroll
+  for (int u = 0; u < kU; ++u) {
+    if (un.ok[u]) {
+      const int sidx = un.h[u] / hl, hloc = un.h[u] - sidx * hl;
+      const uint8_t* src = wire + ((static_cast<int64_t>(sidx) * n_rows + un.r[u]) * hl + hloc) * kRec;
+      if (kFmt == H3_WIRE_BF16) {
+        in[u] = ld8(src + lane * 8);
+      } else {
+        in[u].x = __ldg(reinterpret_cast<const uint32_t*>(src + lane * 4));
+        if (kFmt == H3_WIRE_INT8) codes[u] = src[128 + (lane >> 3)];
+      }
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kU; ++u) {
+    if (!un.ok[u]) break;
+    uint2 o;
+    if (kFmt == H3_WIRE_BF16) o = in[u];
+    else if (kFmt == H3_WIRE_INT8) o = dequant4(in[u].x, codes[u]);
+    else o = fp8x4_to_bf16(in[u].x);
+    *reinterpret_cast<uint2*>(out + un.r[u] * os + un.h[u] * kHeadDim + lane * 4) = o;
   }
 }
 
-unsigned blocks_for(int64_t units) { return static_cast<unsigned>((units + kWarps - 1) / kWarps); }
+// Blocks for `units` (row, head) units at kU units per warp.
+unsigned blocks_for(int64_t units, int ku) {
+  return static_cast<unsigned>((units + kWarps * ku - 1) / (kWarps * ku));
+}
 
 }  // namespace
 
 cudaError_t launch_pack_qkv(const WireQkvArgs& a, cudaStream_t s) {
-  const unsigned g = blocks_for(a.n_rows * a.n_heads);
-  if (a.format == H3_WIRE_BF16)
-    pack_qkv_kernel<H3_WIRE_BF16><<<g, kWarps * 32, 0, s>>>(a.q, a.qs, a.k, a.ks, a.v, a.vs,
-                                                            a.n_rows, a.n_heads, a.n_parts, a.wire);
-  else
-    pack_qkv_kernel<H3_WIRE_INT8><<<g, kWarps * 32, 0, s>>>(a.q, a.qs, a.k, a.ks, a.v, a.vs,
-                                                            a.n_rows, a.n_heads, a.n_parts, a.wire);
+  if (a.format == H3_WIRE_BF16) {
+    pack_qkv_bf16_kernel<<<blocks_for(a.n_rows * a.n_heads, 2), kWarps * 32, 0, s>>>(
+        a.q, a.qs, a.k, a.ks, a.v, a.vs, a.n_rows, a.n_heads, a.n_parts, a.wire);
+    return cudaGetLastError();
+  }
+  // persistent: as many blocks as fit at once, or fewer for a small input
+  static int per_sm_cache[64], sms_cache[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (per_sm_cache[dev] == 0) {
+    int per_sm = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pack_qkv_int8_kernel, kWarps * 32, 0);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    sms_cache[dev] = sms;
+    per_sm_cache[dev] = per_sm < 1 ? 1 : per_sm;
+  }
+  const int64_t full = static_cast<int64_t>(sms_cache[dev]) * per_sm_cache[dev];
+  const int64_t need = blocks_for(a.n_rows * a.n_heads, kInt8PackU);
+  const unsigned g = static_cast<unsigned>(need < full ? need : full);
+  pack_qkv_int8_kernel<<<g, kWarps * 32, 0, s>>>(a.q, a.qs, a.k, a.ks, a.v, a.vs, a.n_rows,
+                                                 a.n_heads, a.n_parts, a.wire);
   return cudaGetLastError();
 }
 
 cudaError_t launch_unpack_qkv(const WireQkvArgs& a, cudaStream_t s) {
-  const unsigned g = blocks_for(a.n_rows * a.n_heads);
+  const unsigned g = blocks_for(a.n_rows * a.n_heads, 2);
   if (a.format == H3_WIRE_BF16)
     unpack_qkv_kernel<H3_WIRE_BF16><<<g, kWarps * 32, 0, s>>>(a.wire, a.n_rows, a.n_heads, a.qm,
                                                               a.qs, a.km, a.ks, a.vm, a.vs);
@@ -254,7 +481,7 @@ cudaError_t launch_unpack_qkv(const WireQkvArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_pack_out(const WireOutArgs& a, cudaStream_t s) {
-  const unsigned g = blocks_for(a.n_rows * a.n_heads);
+  const unsigned g = blocks_for(a.n_rows * a.n_heads, 4);
   switch (a.format) {
     case H3_WIRE_BF16:
       pack_out_kernel<H3_WIRE_BF16><<<g, kWarps * 32, 0, s>>>(a.out, a.os, a.n_rows, a.n_heads, a.wire);
@@ -269,7 +496,7 @@ cudaError_t launch_pack_out(const WireOutArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_merge_heads(const WireOutArgs& a, cudaStream_t s) {
-  const unsigned g = blocks_for(a.n_rows * a.n_heads);
+  const unsigned g = blocks_for(a.n_rows * a.n_heads, 4);
   switch (a.format) {
     case H3_WIRE_BF16:
       merge_heads_kernel<H3_WIRE_BF16><<<g, kWarps * 32, 0, s>>>(a.wire, a.n_rows, a.n_heads,

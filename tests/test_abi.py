@@ -193,6 +193,7 @@ def test_wire_record_sizes_on_host(lib):
 @pytest.mark.parametrize("args,code", [
     (dict(nd=4), ARG), (dict(nd=0), ARG), (dict(fmt=2), ARG), (dict(q=None), ARG),
     (dict(q=A + 4), ALIGN), (dict(ks=5375), SHAPE), (dict(wire=A + 8), ALIGN), (dict(H=0), ARG),
+    (dict(n=2 ** 33), ARG), (dict(n=-1), ARG),
 ])
 def test_pack_qkv_rejects_on_host(lib, args, code):
     a = dict(q=A, qs=5376, k=A, ks=5376, v=A, vs=5376, n=10, H=42, nd=2, fmt=1, wire=A)
@@ -203,7 +204,7 @@ def test_pack_qkv_rejects_on_host(lib, args, code):
 
 @pytest.mark.parametrize("args,code", [
     (dict(ns=5), ARG), (dict(fmt=3), ARG), (dict(o=None), ARG), (dict(os_=100), SHAPE),
-    (dict(wire=None), ARG), (dict(wire=A + 4), ALIGN),
+    (dict(wire=None), ARG), (dict(wire=A + 4), ALIGN), (dict(n=2 ** 33), ARG),
 ])
 def test_merge_heads_rejects_on_host(lib, args, code):
     a = dict(wire=A, n=10, H=42, ns=2, fmt=2, o=A, os_=5376)

@@ -106,3 +106,40 @@ def test_output_records_and_head_merge(fmt, n_src):
 def test_wire_record_sizes():
     assert [h3.wire_record_bytes("qkv", f) for f in (0, 1)] == [768, 400]
     assert [h3.wire_record_bytes("out", f) for f in (0, 1, 2)] == [256, 144, 128]
+
+
+def hard_int8_values(rows, H, seed):
+    """bf16 [rows, H, 128] whose 32-value groups stress the INT8 encoder:
+    exact half-integer quotients x / value(c) (rounding ties) at every scale
+    code, groups whose max sits exactly on 127 * value(c), values past the
+    largest code (saturation), subnormal and all-zero groups."""
+    rng = np.random.default_rng(seed)
+    n_groups = rows * H * 4
+    codes = rng.integers(0, 256, n_groups)
+    s = O.ue5m3_value(codes)[:, None]
+    kind = rng.integers(0, 5, n_groups)[:, None]
+    j = rng.integers(-127, 127, (n_groups, 32)).astype(np.float64)
+    x = np.where(kind == 0, (j + 0.5) * s, j * s)                       # ties / grid points
+    x = np.where(kind == 2, x * 3.0e4, x)                                # saturation
+    x = np.where(kind == 3, rng.standard_normal((n_groups, 32)) * 1e-39, x)  # subnormal bf16
+    x = np.where((kind == 4) & (rng.random((n_groups, 1)) < 0.2), 0.0, x)
+    edge = (kind == 1)[:, 0] & (codes % 8 == 0)
+    x[edge, 0] = 127.0 * s[edge, 0]                                      # amax on a boundary
+    t = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).reshape(rows, H, 128)
+    return t
+
+
+def test_int8_encoder_hard_values():
+    rows, H = 160, 6
+    q, k, v = (hard_int8_values(rows, H, seed).cuda() for seed in (11, 12, 13))
+    qq, kk, vv = O.widen(q), O.widen(k), O.widen(v)
+    ties = np.abs(qq.reshape(-1, 32)) / O.ue5m3_value(
+        O.ue5m3_scale_code(np.abs(qq.reshape(-1, 32)).max(-1)))[:, None]
+    assert np.any(ties % 1.0 == 0.5) and np.any(ties > 127)  # the cases above survive bf16
+    wire = h3.pack_qkv(q, k, v, 2, h3.WIRE_INT8)
+    out = h3.pack_out(q, h3.WIRE_INT8)
+    torch.cuda.synchronize()
+    for d in range(2):
+        hs = slice(d * 3, d * 3 + 3)
+        assert np.array_equal(as_bytes(wire[d]), O.qkv_int8_records(qq[:, hs], kk[:, hs], vv[:, hs]))
+    assert np.array_equal(as_bytes(out), O.out_int8_records(qq))
