@@ -193,6 +193,16 @@ def bench_gpu(args):
     # ---- device-resident inputs (seeded, generated on the GPU)
     g = W.make_inputs(w, device=f"cuda:{local}", seed=W.default_seed(w) + rank)
     stream = torch.cuda.current_stream()
+    if args.wire_only:
+        if not w.self_attention:
+            raise SystemExit("--wire-only needs a self-attention workload")
+        res = wire_timing(h3, g, w, stream, pk)
+        if rank == 0:
+            print(json.dumps({"workload": w.name, "rows": w.segments[0].n_valid_q(),
+                              "wire_formats": res}))
+        if dist is not None:
+            dist.destroy_process_group()
+        return
     for _ in range(args.warmup):
         run_step(h3, g, w)
     torch.cuda.synchronize()
@@ -571,6 +581,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernels-only", action="store_true",
                     help="profiling mode: warm-up and timed steps only (no e2e, no CPU baseline)")
+    ap.add_argument("--wire-only", action="store_true",
+                    help="profiling mode: the wire-format kernels on the first sequence only")
     args = ap.parse_args()
     if args.impl == "reference":
         bench_reference(args)
