@@ -61,9 +61,8 @@ constexpr uint32_t kOffV = kOffK + kNS * kTileBytes;
 constexpr uint32_t kOffBar = kOffV + kNS * kTileBytes;
 enum {
   BAR_Q = 0,
-  BAR_KFULL = 1,
-  BAR_VFULL = BAR_KFULL + kNS,
-  BAR_KVEMPTY = BAR_VFULL + kNS,
+  BAR_KVFULL = 1,  // K and V of a ring stage landed (one barrier: fewer waits for the issuer)
+  BAR_KVEMPTY = BAR_KVFULL + kNS,
   BAR_SFULL = BAR_KVEMPTY + kNS,
   BAR_PFULL = BAR_SFULL + 2,
   BAR_OFINAL = BAR_PFULL + 2,
@@ -296,8 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   if (threadIdx.x == 0) {
     mbar_init(bar(BAR_Q), 1);
     for (int s = 0; s < kNS; ++s) {
-      mbar_init(bar(BAR_KFULL + s), 1);
-      mbar_init(bar(BAR_VFULL + s), 1);
+      mbar_init(bar(BAR_KVFULL + s), 1);
       mbar_init(bar(BAR_KVEMPTY + s), 1);
     }
     for (int t = 0; t < 2; ++t) {
@@ -354,13 +352,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const CUtensorMap* tk = first ? tk1 : tk2;
         const CUtensorMap* tv = first ? tv1 : tv2;
         const int row = (kSparse ? static_cast<int>(list_tiles[j]) : (first ? j : j - n_kv1)) * kBN;
-        mbar_arrive_expect_tx(bar(BAR_KFULL + s), kTileBytes);
+        mbar_arrive_expect_tx(bar(BAR_KVFULL + s), 2 * kTileBytes);
         for (int h = 0; h < 2; ++h)
-          tma_load_3d(sbase + kOffK + s * kTileBytes + h * kHalfBytes, tk, bar(BAR_KFULL + s),
+          tma_load_3d(sbase + kOffK + s * kTileBytes + h * kHalfBytes, tk, bar(BAR_KVFULL + s),
                       h * 64, head, row);
-        mbar_arrive_expect_tx(bar(BAR_VFULL + s), kTileBytes);
         for (int h = 0; h < 2; ++h)
-          tma_load_3d(sbase + kOffV + s * kTileBytes + h * kHalfBytes, tv, bar(BAR_VFULL + s),
+          tma_load_3d(sbase + kOffV + s * kTileBytes + h * kHalfBytes, tv, bar(BAR_KVFULL + s),
                       h * 64, head, row);
         armed[s] = use;
       }
@@ -369,8 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         drain_wait(bar(BAR_Q), 0);
         for (int s = 0; s < kNS; ++s)
           if (armed[s] >= 0) {
-            drain_wait(bar(BAR_KFULL + s), armed[s] & 1);
-            drain_wait(bar(BAR_VFULL + s), armed[s] & 1);
+            drain_wait(bar(BAR_KVFULL + s), armed[s] & 1);
           }
       }
     }
@@ -401,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
       };
       bool ok = wait1(bar(BAR_Q), 0, wctx, H3_STATUS_TIMEOUT_MMA) &&
-                wait1(bar(BAR_KFULL), 0, wctx, H3_STATUS_TIMEOUT_MMA);
+                wait1(bar(BAR_KVFULL), 0, wctx, H3_STATUS_TIMEOUT_MMA);
       if (ok) {
         tc_fence_after();
         for (int t = 0; t < n_tiles; ++t) {
@@ -409,28 +405,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           mma_commit(bar(BAR_SFULL + t));
         }
       }
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int s = j % kNS, use = j / kNS;
-        const int s2 = (j + 1) % kNS, use2 = (j + 1) / kNS;
-        const bool next = j + 1 < n_kv;
-        ok = wait1(bar(BAR_VFULL + s), use & 1, wctx, H3_STATUS_TIMEOUT_MMA);
-        for (int t = 0; t < n_tiles && ok; ++t) {
-          ok = wait1(bar(BAR_PFULL + t), j & 1, wctx, H3_STATUS_TIMEOUT_MMA);
-          if (!ok) break;
-          tc_fence_after();
-          pv(t, s, j > 0);
-          if (t == n_tiles - 1) mma_commit(bar(BAR_KVEMPTY + s));
-          if (next) {
-            if (t == 0) {
-              ok = wait1(bar(BAR_KFULL + s2), use2 & 1, wctx, H3_STATUS_TIMEOUT_MMA);
-              if (!ok) break;
-              tc_fence_after();
-            }
-            qk(t, s2);
-            mma_commit(bar(BAR_SFULL + t));
-          } else {
-            mma_commit(bar(BAR_OFINAL + t));
+      // One flat loop over (KV step j, query tile t) groups keeps the
+      // issuer's path short and identical for every group: wait for P_t(j),
+      // P_t(j).V(j), then (K/V of step j + 1 landed) Q_t.K(j + 1)^T.  V(j)
+      // landed with K(j), which the previous group already waited for.
+      const int n_groups = n_kv * n_tiles;
+      for (int g = 0; g < n_groups && ok; ++g) {
+        const int j = n_tiles == 2 ? (g >> 1) : g;
+        const int t = g - j * n_tiles;
+        const int s = j % kNS, s2 = (j + 1) % kNS, use2 = (j + 1) / kNS;
+        ok = wait1(bar(BAR_PFULL + t), j & 1, wctx, H3_STATUS_TIMEOUT_MMA);
+        if (!ok) break;
+        tc_fence_after();
+        pv(t, s, j > 0);
+        if (t == n_tiles - 1) mma_commit(bar(BAR_KVEMPTY + s));
+        if (j + 1 < n_kv) {
+          if (t == 0) {
+            ok = wait1(bar(BAR_KVFULL + s2), use2 & 1, wctx, H3_STATUS_TIMEOUT_MMA);
+            if (!ok) break;
+            tc_fence_after();
           }
+          qk(t, s2);
+          mma_commit(bar(BAR_SFULL + t));
+        } else {
+          mma_commit(bar(BAR_OFINAL + t));
         }
       }
       // Every MMA issued above completes before TMEM is released.
