@@ -292,6 +292,21 @@ int h3_pack_out(const void* out, int64_t out_row_stride, int64_t n_rows, int n_h
 int h3_merge_heads(const void* wire, int64_t n_rows, int n_heads, int n_src, int format, void* out,
                    int64_t out_row_stride, h3_stream_t stream);
 
+/*
+ * Strided transfer helper (not a step of the method): copies `height` rows
+ * of `width_bytes` bytes from src (row pitch src_pitch bytes) to dst (row
+ * pitch dst_pitch bytes), asynchronously on `stream`, in whichever direction
+ * the two addresses imply (host <-> device or device <-> device).  Used to
+ * move a group of heads of a [rows, heads, 128] tensor between pinned host
+ * memory and the device while other heads are being computed.  Host memory
+ * must be pinned for the copy to be asynchronous.  Returns H3_ERR_ARG for a
+ * NULL pointer or a negative extent, H3_ERR_SHAPE for a pitch below the
+ * width, H3_ERR_LAUNCH when the runtime rejects the copy; an empty copy
+ * returns H3_OK without touching either pointer.
+ */
+int h3_copy_2d(void* dst, int64_t dst_pitch, const void* src, int64_t src_pitch,
+               int64_t width_bytes, int64_t height, h3_stream_t stream);
+
 /* Message for the last nonzero status returned to the calling thread
  * ("" if none).  The pointer stays valid until the thread's next call. */
 const char* h3_last_error(void);

@@ -336,6 +336,91 @@ def attention_block(q, k, v, wq, wk, pos_thw, cu_seqlens, valid_len,
     return attention(q, k, v, cu_seqlens, cu_seqlens, valid_len, scale, out, stream)
 
 
+def copy_2d(dst: torch.Tensor, src: torch.Tensor, stream=None) -> None:
+    """Asynchronous copy between two [rows, heads, 128] views with the same
+    shape (for instance one group of heads of a pinned host tensor and of a
+    device tensor); each row's heads must be contiguous."""
+    if dst.shape != src.shape or dst.dtype != src.dtype:
+        raise ValueError(f"copy_2d: shapes/dtypes differ ({tuple(dst.shape)} vs {tuple(src.shape)})")
+    es = dst.element_size()
+    width = dst.shape[1] * dst.shape[2] * es
+    for t, name in ((dst, "dst"), (src, "src")):
+        if t.stride(2) != 1 or (t.shape[1] > 1 and t.stride(1) != t.shape[2]):
+            raise ValueError(f"copy_2d: {name} must hold each row's heads contiguously")
+    _check(lib().h3_copy_2d(dst.data_ptr(), dst.stride(0) * es, src.data_ptr(),
+                            src.stride(0) * es, width, dst.shape[0], _stream(stream)))
+
+
+class HostPipeline:
+    """The block's hot path on inputs in pinned host memory, with the
+    transfers hidden behind the compute.
+
+    Heads are processed in groups: the Q/K/V rows of group g + 1 are copied
+    host -> device while group g is normalised and attended, and group g's
+    output is copied back as soon as it is done.  Consecutive groups run on
+    two compute streams so that one attention launch's last partial wave
+    overlaps the next launch.  Heads are independent, so the result is
+    bitwise that of ``attention_block`` on the whole tensors.
+
+    The device buffers (Q, K, V, out, weights, positions) are allocated once
+    for ``rows`` x ``n_heads``; host tensors must be pinned and shaped like
+    them.
+    """
+
+    def __init__(self, rows: int, n_heads: int, heads_per_group: int = 6, device=None):
+        dev = torch.device(device if device is not None else "cuda")
+        bf = torch.bfloat16
+        self.rows, self.n_heads = rows, n_heads
+        self.q = torch.empty((rows, n_heads, HEAD_DIM), dtype=bf, device=dev)
+        self.k = torch.empty_like(self.q)
+        self.v = torch.empty_like(self.q)
+        self.out = torch.empty_like(self.q)
+        self.wq = torch.empty((n_heads, HEAD_DIM), dtype=bf, device=dev)
+        self.wk = torch.empty_like(self.wq)
+        self.pos = torch.empty((rows, 3), dtype=torch.int32, device=dev)
+        g = max(1, min(heads_per_group, n_heads))
+        self.groups = [(h, min(h + g, n_heads)) for h in range(0, n_heads, g)]
+        self.s_in = torch.cuda.Stream(device=dev)
+        self.s_out = torch.cuda.Stream(device=dev)
+        self.s_comp = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
+
+    def run(self, q, k, v, wq, wk, pos_thw, cu_seqlens, valid_len, out,
+            rot=(32, 48, 48), theta=10000.0, eps=1e-6, scale=None, stream=None) -> None:
+        """Queue one block step after the work already on ``stream`` (default:
+        the current stream); ``stream`` waits for the whole step, so a
+        synchronise on it (or an event recorded on it) sees ``out`` filled.
+        Q, K, V, weights and positions are read from the host tensors; the
+        device copies of Q and K are normalised in place."""
+        cur = stream if stream is not None else torch.cuda.current_stream()
+        start = torch.cuda.Event()
+        start.record(cur)
+        for s in (self.s_in, self.s_out, *self.s_comp):
+            s.wait_event(start)
+        with torch.cuda.stream(self.s_in):
+            self.wq.copy_(wq, non_blocking=True)
+            self.wk.copy_(wk, non_blocking=True)
+            self.pos.copy_(pos_thw, non_blocking=True)
+        for i, (h0, h1) in enumerate(self.groups):
+            for dev_t, host_t in ((self.q, q), (self.k, k), (self.v, v)):
+                copy_2d(dev_t[:, h0:h1], host_t[:, h0:h1], self.s_in)
+            landed = torch.cuda.Event()
+            landed.record(self.s_in)
+            sc = self.s_comp[i % 2]
+            sc.wait_event(landed)
+            attention_block(self.q[:, h0:h1], self.k[:, h0:h1], self.v[:, h0:h1],
+                            self.wq[h0:h1], self.wk[h0:h1], self.pos, cu_seqlens, valid_len,
+                            rot=rot, theta=theta, eps=eps, scale=scale,
+                            out=self.out[:, h0:h1], stream=sc)
+            done = torch.cuda.Event()
+            done.record(sc)
+            self.s_out.wait_event(done)
+            copy_2d(out[:, h0:h1], self.out[:, h0:h1], self.s_out)
+        for s in (self.s_out, *self.s_comp):
+            ev = torch.cuda.Event()
+            ev.record(s)
+            cur.wait_event(ev)
+
+
 def status_word() -> int:
     """Synchronise the device; return and clear the device status bits
     (0 = no bounded wait gave up since the last read)."""

@@ -51,6 +51,7 @@ SIGNATURES = {
     "h3_pack_out": (c_int, [c_void_p, c_int64, c_int64, c_int, c_int, c_void_p, c_void_p]),
     "h3_merge_heads": (c_int, [c_void_p, c_int64, c_int, c_int, c_int, c_void_p, c_int64,
                                c_void_p]),
+    "h3_copy_2d": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_int64, c_int64, c_void_p]),
     "h3_last_error": (ctypes.c_char_p, []),
     "h3_status_word": (c_int, [c_u32p]),
     "h3_version": (c_int, []),

@@ -524,6 +524,22 @@ int h3_merge_heads(const void* wire, int64_t n_rows, int n_heads, int n_src, int
   return H3_OK;
 }
 
+int h3_copy_2d(void* dst, int64_t dst_pitch, const void* src, int64_t src_pitch,
+               int64_t width_bytes, int64_t height, h3_stream_t stream) {
+  if (height < 0 || width_bytes < 0) return fail(H3_ERR_ARG, "negative copy extent");
+  if (height == 0 || width_bytes == 0) return H3_OK;
+  if (!dst || !src) return fail(H3_ERR_ARG, "dst and src must not be NULL");
+  if (dst_pitch < width_bytes || src_pitch < width_bytes)
+    return fail(H3_ERR_SHAPE, "pitches (%lld, %lld) must be >= the width (%lld)",
+                (long long)dst_pitch, (long long)src_pitch, (long long)width_bytes);
+  const cudaError_t e =
+      cudaMemcpy2DAsync(dst, static_cast<size_t>(dst_pitch), src, static_cast<size_t>(src_pitch),
+                        static_cast<size_t>(width_bytes), static_cast<size_t>(height),
+                        cudaMemcpyDefault, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(H3_ERR_LAUNCH, "2-D copy: %s", cudaGetErrorString(e));
+  return H3_OK;
+}
+
 int h3_status_word(uint32_t* out) {
   if (!out) return fail(H3_ERR_ARG, "out must not be NULL");
   cudaError_t e = h3::read_and_clear_status(out);

@@ -213,6 +213,21 @@ def test_merge_heads_rejects_on_host(lib, args, code):
                               None) == code
 
 
+@pytest.mark.parametrize("args,code", [
+    (dict(dst=None), ARG), (dict(src=None), ARG), (dict(h=-1), ARG), (dict(w=-4), ARG),
+    (dict(dp=100), SHAPE), (dict(sp=100), SHAPE),
+])
+def test_copy_2d_rejects_on_host(lib, args, code):
+    a = dict(dst=A, dp=10752, src=A, sp=10752, w=1536, h=10)
+    a.update(args)
+    assert lib.h3_copy_2d(a["dst"], a["dp"], a["src"], a["sp"], a["w"], a["h"], None) == code
+
+
+def test_copy_2d_empty_is_a_no_op(lib):
+    assert lib.h3_copy_2d(None, 0, None, 0, 1536, 0, None) == 0
+    assert lib.h3_copy_2d(None, 0, None, 0, 0, 10, None) == 0
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
 def test_valid_call_without_gpu_reports_device_error(lib):
     assert attn(lib) == DEVICE
