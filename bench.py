@@ -291,21 +291,27 @@ def bench_gpu(args):
     for _ in range(min(args.warmup, 2)):
         e2e_step()
     torch.cuda.synchronize()
-    e_start = torch.cuda.Event(enable_timing=True)
-    e_end = torch.cuda.Event(enable_timing=True)
-    e_steps = max(1, min(args.steps, 5))
+    # Each step is timed on its own (a step waits for the previous one to
+    # finish, so steps do not overlap).  Host <-> device copies occasionally
+    # stall for tens of milliseconds independently of this program; the
+    # median step is the value, the mean and the slowest step are reported
+    # beside it.
+    e_steps = max(5, min(args.steps, 10))
+    e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(e_steps + 1)]
     if dist is not None:
         dist.barrier()
-    e_start.record(stream)
-    for _ in range(e_steps):
+    e_ev[0].record(stream)
+    for i in range(e_steps):
         e2e_step()
-    e_end.record(stream)
+        e_ev[i + 1].record(stream)
     torch.cuda.synchronize()
-    e_ms = e_start.elapsed_time(e_end) / e_steps
+    e_each = [e_ev[i].elapsed_time(e_ev[i + 1]) for i in range(e_steps)]
+    e_ms = float(np.median(e_each))
+    e_mean = float(np.mean(e_each))
     if dist is not None:
-        t = torch.tensor([e_ms], device="cuda")
+        t = torch.tensor([e_ms, e_mean], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e_ms = float(t.item())
+        e_ms, e_mean = float(t[0].item()), float(t[1].item())
     e2e_value = flops * world / (e_ms * 1e-3) / 1e12
 
     if rank != 0:
@@ -360,6 +366,9 @@ def bench_gpu(args):
                       "sol_block_sparse": sol, "wire_formats": wire},
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 3),
+                "statistic": f"median of {len(e_each)} individually timed steps",
+                "mean_ms_per_step": round(e_mean, 3), "max_ms_per_step": round(max(e_each), 3),
+                "value_at_mean": round(flops * world / (e_mean * 1e-3) / 1e12, 3),
                 "path": (f"HostPipeline: {len(pipe.groups)} head groups, copies overlapped with compute"
                          if pipe is not None else "copy in, step, copy out")},
         "gpu_launches": launches_per_step(w) * args.steps,
