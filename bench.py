@@ -98,6 +98,25 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ------------------------------------------------------- replicas (N > 1)
+def max_over_ranks(values, dist, device):
+    """Element-wise maximum of per-rank timings over all ranks: the slowest
+    rank decides.  ``dist`` is torch.distributed (any backend) or None."""
+    if dist is None:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_value(units_per_rank, ms_per_step, world):
+    """Whole-job throughput in units/s x 1e-12 (TFLOP/s for FLOP): the units
+    every rank processed in one step over the slowest rank's step time.
+    Ranks are independent replicas with the same per-rank work (weak
+    scaling)."""
+    return units_per_rank * world / (ms_per_step * 1e-3) / 1e12
+
+
 # -------------------------------------------------------------- the GPU arm
 def launches_per_step(w):
     return (len([s for s in w.segments if s.n_valid_q() > 0]) if w.self_attention else 0) + 1
@@ -247,13 +266,10 @@ def bench_gpu(args):
     status = h3.status_word()
     if status:
         raise SystemExit(f"device status word {status:#x} after the timed region")
-    if dist is not None:
-        t = torch.tensor([ms_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks([ms_total], dist, "cuda")[0]
     ms_step = ms_total / args.steps
     flops = w.attention_flops()
-    value = flops * world / (ms_step * 1e-3) / 1e12
+    value = whole_job_value(flops, ms_step, world)
     attn_tflops = flops / (attn_ms * 1e-3) / 1e12
     pro_gbs = w.prologue_bytes() / (pro_ms * 1e-3) / 1e9 if pro_ms > 0 else None
 
@@ -308,11 +324,8 @@ def bench_gpu(args):
     e_each = [e_ev[i].elapsed_time(e_ev[i + 1]) for i in range(e_steps)]
     e_ms = float(np.median(e_each))
     e_mean = float(np.mean(e_each))
-    if dist is not None:
-        t = torch.tensor([e_ms, e_mean], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e_ms, e_mean = float(t[0].item()), float(t[1].item())
-    e2e_value = flops * world / (e_ms * 1e-3) / 1e12
+    e_ms, e_mean = max_over_ranks([e_ms, e_mean], dist, "cuda")
+    e2e_value = whole_job_value(flops, e_ms, world)
 
     if rank != 0:
         dist.barrier()
@@ -368,7 +381,7 @@ def bench_gpu(args):
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 3),
                 "statistic": f"median of {len(e_each)} individually timed steps",
                 "mean_ms_per_step": round(e_mean, 3), "max_ms_per_step": round(max(e_each), 3),
-                "value_at_mean": round(flops * world / (e_mean * 1e-3) / 1e12, 3),
+                "value_at_mean": round(whole_job_value(flops, e_mean, world), 3),
                 "path": (f"HostPipeline: {len(pipe.groups)} head groups, copies overlapped with compute"
                          if pipe is not None else "copy in, step, copy out")},
         "gpu_launches": launches_per_step(w) * args.steps,
