@@ -544,12 +544,21 @@ def wire_timing(h3, g, w, stream, pk, iters=5):
     return res
 
 
+def kernel_source_digest():
+    """First 16 hex digits of sha256 over the attention kernel's device code:
+    attention.cu up to its host-side section, then ptx.cuh."""
+    import hashlib
+    csrc = os.path.join(ROOT, "packed_sequence_attention_gb300", "csrc")
+    text = open(os.path.join(csrc, "attention.cu"), "rb").read()
+    cut = text.find(b"// ------------------------------------------------------------------ host side")
+    device = text if cut < 0 else text[:cut]
+    return hashlib.sha256(device + open(os.path.join(csrc, "ptx.cuh"), "rb").read()).hexdigest()[:16]
+
+
 def committed_traffic(w):
     """DRAM bytes per attention launch from the committed ncu summary, if it
-    was taken on this workload and on the current kernel source."""
-    import hashlib
+    was taken on this workload and on the current kernel device code."""
     path = os.path.join(ROOT, "profiles", "attention_traffic.txt")
-    src = os.path.join(ROOT, "packed_sequence_attention_gb300", "csrc", "attention.cu")
     if not os.path.exists(path):
         return None
     kv = {}
@@ -557,8 +566,7 @@ def committed_traffic(w):
         if ":" in line and not line.startswith("#"):
             a, b = line.split(":", 1)
             kv[a.strip()] = b.strip()
-    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    if kv.get("source_sha256_16") != digest or kv.get("workload") != w.name:
+    if kv.get("kernel_source_sha256_16") != kernel_source_digest() or kv.get("workload") != w.name:
         return None
     try:
         return float(kv["dram_bytes_per_launch"])

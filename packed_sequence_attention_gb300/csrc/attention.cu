@@ -593,9 +593,8 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn get_encoder(std::string& err) {
-  static EncodeTiledFn fn = nullptr;
-  static std::atomic<int> state{0};
-  if (state.load() == 1) return fn;
+  static std::atomic<EncodeTiledFn> fn{nullptr};
+  if (EncodeTiledFn f = fn.load()) return f;
   void* ptr = nullptr;
   cudaDriverEntryPointQueryResult q{};
   cudaError_t e =
@@ -604,9 +603,9 @@ EncodeTiledFn get_encoder(std::string& err) {
     err = std::string("cuTensorMapEncodeTiled unavailable: ") + cudaGetErrorString(e);
     return nullptr;
   }
-  fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  state.store(1);
-  return fn;
+  const EncodeTiledFn f = reinterpret_cast<EncodeTiledFn>(ptr);
+  fn.store(f);  // threads racing here store the same entry point
+  return f;
 }
 
 // [rows, n_heads, 128] bf16 starting at `base`, boxes of 64 channels x 1 head x 128 rows.
@@ -804,15 +803,14 @@ int launch_sparse_attention(const SparseAttnArgs& a, cudaStream_t stream, std::s
 // Device address of the status word on the current device (looked up once
 // per device, with that device current), for kernels in other files.
 uint32_t* status_word_device_ptr() {
-  static uint32_t* ptrs[64];
+  static std::atomic<uint32_t*> ptrs[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (ptrs[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
-    ptrs[dev] = static_cast<uint32_t*>(p);
-  }
-  return ptrs[dev];
+  if (uint32_t* q = ptrs[dev].load()) return q;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+  ptrs[dev].store(static_cast<uint32_t*>(p));  // racing threads store the same address
+  return static_cast<uint32_t*>(p);
 }
 
 cudaError_t read_and_clear_status(uint32_t* out) {

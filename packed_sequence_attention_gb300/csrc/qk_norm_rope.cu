@@ -25,6 +25,7 @@
 // * Every mbarrier wait is bounded; a wait that gives up sets a bit in the
 //   device status word and the CTA stops.
 #include <cmath>
+#include <mutex>
 
 #include "h3_internal.h"
 #include "ptx.cuh"
@@ -290,16 +291,22 @@ cudaError_t launch_qk_norm_rope(const NormRopeArgs& a, cudaStream_t stream) {
   p.n_stages = nst;
   const size_t smem = nst * (stage_bytes + 64 * 8) + kMaxStages * 8;
   auto kernel = lora ? qk_norm_rope_kernel<true> : qk_norm_rope_kernel<false>;
-  static size_t attr_smem[2][64];
+  // The attribute only ever grows, so a launch never runs under a smaller
+  // limit that another thread set after it checked.
+  static std::mutex attr_mu;
+  static size_t attr_smem[2][64];  // guarded by attr_mu
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (attr_smem[lora][dev] < smem) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    attr_smem[lora][dev] = smem;
+  {
+    std::lock_guard<std::mutex> lock(attr_mu);
+    if (attr_smem[lora][dev] < smem) {
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+      attr_smem[lora][dev] = smem;
+    }
   }
   int per_sm = 0, sms = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem);

@@ -21,6 +21,8 @@
 // three xor-shuffles.
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "h3_internal.h"
 #include "ptx.cuh"
 
@@ -447,21 +449,23 @@ cudaError_t launch_pack_qkv(const WireQkvArgs& a, cudaStream_t s) {
     return cudaGetLastError();
   }
   // persistent: as many blocks as fit at once, or fewer for a small input
-  static int per_sm_cache[64], sms_cache[64];
+  // resident blocks of the whole device, looked up once per device (racing
+  // threads store the same value)
+  static std::atomic<int64_t> full_cache[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (per_sm_cache[dev] == 0) {
+  int64_t full = full_cache[dev].load();
+  if (full == 0) {
     int per_sm = 0, sms = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pack_qkv_int8_kernel, kWarps * 32, 0);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    sms_cache[dev] = sms;
-    per_sm_cache[dev] = per_sm < 1 ? 1 : per_sm;
+    full = static_cast<int64_t>(sms) * (per_sm < 1 ? 1 : per_sm);
+    full_cache[dev].store(full);
   }
-  const int64_t full = static_cast<int64_t>(sms_cache[dev]) * per_sm_cache[dev];
   const int64_t need = blocks_for(a.n_rows * a.n_heads, kInt8PackU);
   const unsigned g = static_cast<unsigned>(need < full ? need : full);
   pack_qkv_int8_kernel<<<g, kWarps * 32, 0, s>>>(a.q, a.qs, a.k, a.ks, a.v, a.vs, a.n_rows,
