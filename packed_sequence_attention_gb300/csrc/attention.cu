@@ -398,38 +398,82 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       };
       bool ok = wait1(bar(BAR_Q), 0, wctx, H3_STATUS_TIMEOUT_MMA) &&
                 wait1(bar(BAR_KVFULL), 0, wctx, H3_STATUS_TIMEOUT_MMA);
-      if (ok) {
-        tc_fence_after();
-        for (int t = 0; t < n_tiles; ++t) {
-          qk(t, 0);
-          mma_commit(bar(BAR_SFULL + t));
-        }
-      }
-      // One flat loop over (KV step j, query tile t) groups keeps the
-      // issuer's path short and identical for every group: wait for P_t(j),
-      // P_t(j).V(j), then (K/V of step j + 1 landed) Q_t.K(j + 1)^T.  V(j)
-      // landed with K(j), which the previous group already waited for.
-      const int n_groups = n_kv * n_tiles;
-      for (int g = 0; g < n_groups && ok; ++g) {
-        const int j = n_tiles == 2 ? (g >> 1) : g;
-        const int t = g - j * n_tiles;
-        const int s = j % kNS, s2 = (j + 1) % kNS, use2 = (j + 1) / kNS;
-        ok = wait1(bar(BAR_PFULL + t), j & 1, wctx, H3_STATUS_TIMEOUT_MMA);
-        if (!ok) break;
-        tc_fence_after();
-        pv(t, s, j > 0);
-        if (t == n_tiles - 1) mma_commit(bar(BAR_KVEMPTY + s));
-        if (j + 1 < n_kv) {
-          if (t == 0) {
-            ok = wait1(bar(BAR_KVFULL + s2), use2 & 1, wctx, H3_STATUS_TIMEOUT_MMA);
-            if (!ok) break;
-            tc_fence_after();
+      if constexpr (!kSparse) {
+        if (ok) {
+          tc_fence_after();
+          for (int t = 0; t < n_tiles; ++t) {
+            qk(t, 0);
+            mma_commit(bar(BAR_SFULL + t));
           }
-          qk(t, s2);
-          mma_commit(bar(BAR_SFULL + t));
-        } else {
-          mma_commit(bar(BAR_OFINAL + t));
         }
+        // One flat loop over (KV step j, query tile t) groups keeps the
+        // issuer's path short and identical for every group: wait for P_t(j),
+        // P_t(j).V(j), then (K/V of step j + 1 landed) Q_t.K(j + 1)^T.  V(j)
+        // landed with K(j), which the previous group already waited for.
+        const int n_groups = n_kv * n_tiles;
+        for (int g = 0; g < n_groups && ok; ++g) {
+          const int j = n_tiles == 2 ? (g >> 1) : g;
+          const int t = g - j * n_tiles;
+          const int s = j % kNS, s2 = (j + 1) % kNS, use2 = (j + 1) / kNS;
+          ok = wait1(bar(BAR_PFULL + t), j & 1, wctx, H3_STATUS_TIMEOUT_MMA);
+          if (!ok) break;
+          tc_fence_after();
+          pv(t, s, j > 0);
+          if (t == n_tiles - 1) mma_commit(bar(BAR_KVEMPTY + s));
+          if (j + 1 < n_kv) {
+            if (t == 0) {
+              ok = wait1(bar(BAR_KVFULL + s2), use2 & 1, wctx, H3_STATUS_TIMEOUT_MMA);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            qk(t, s2);
+            mma_commit(bar(BAR_SFULL + t));
+          } else {
+            mma_commit(bar(BAR_OFINAL + t));
+          }
+        }
+      } else {
+        // Block-sparse: the steps walk the union of the two tiles' lists; a
+        // tile takes part only in the steps its own list keeps (no MMA for
+        // the others).  Its S/P barrier phases count its kept steps.
+        auto keeps = [&](int t, int j) -> bool { return t < n_tiles && ((list_sel[j] >> t) & 1u); };
+        int kept[2] = {0, 0};
+        if (ok) {
+          tc_fence_after();
+          for (int t = 0; t < n_tiles; ++t)
+            if (keeps(t, 0)) {
+              qk(t, 0);
+              mma_commit(bar(BAR_SFULL + t));
+            }
+        }
+        for (int j = 0; j < n_kv && ok; ++j) {
+          const int s = j % kNS, s2 = (j + 1) % kNS, use2 = (j + 1) / kNS;
+          const int last = keeps(1, j) ? 1 : 0;  // the last tile that reads stage s
+          bool next_landed = false;
+          for (int t = 0; t < n_tiles && ok; ++t) {
+            if (keeps(t, j)) {
+              ok = wait1(bar(BAR_PFULL + t), kept[t] & 1, wctx, H3_STATUS_TIMEOUT_MMA);
+              if (!ok) break;
+              tc_fence_after();
+              pv(t, s, kept[t] > 0);
+              ++kept[t];
+            }
+            if (t == last) mma_commit(bar(BAR_KVEMPTY + s));
+            if (j + 1 < n_kv && keeps(t, j + 1)) {
+              if (!next_landed) {
+                ok = wait1(bar(BAR_KVFULL + s2), use2 & 1, wctx, H3_STATUS_TIMEOUT_MMA);
+                if (!ok) break;
+                tc_fence_after();
+                next_landed = true;
+              }
+              qk(t, s2);
+              mma_commit(bar(BAR_SFULL + t));
+            }
+          }
+        }
+        if (ok)
+          for (int t = 0; t < n_tiles; ++t)
+            if (kept[t] > 0) mma_commit(bar(BAR_OFINAL + t));
       }
       // Every MMA issued above completes before TMEM is released.
       mma_commit(bar(BAR_DRAIN));
@@ -458,8 +502,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       float m_used = -INFINITY;
       float l = 0.0f;
       bool ok = true;
+      int kept = 0;  // KV steps this tile has processed (= j in dense mode)
       for (int j = 0; j < n_kv; ++j) {
-        ok = wait_warp(bar(BAR_SFULL + t), j & 1, wctx, H3_STATUS_TIMEOUT_SOFTMAX);
+        // Block-sparse: steps this tile's list does not keep have no S / P.
+        if (kSparse && !((list_sel[j] >> t) & 1u)) continue;
+        ok = wait_warp(bar(BAR_SFULL + t), kept & 1, wctx, H3_STATUS_TIMEOUT_SOFTMAX);
         if (!ok) break;
         tc_fence_after();
         float s[4][32];
@@ -467,19 +514,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, s[q]);
 #pragma unroll
         for (int q = 0; q < 4; ++q) tmem_wait_ld(s[q]);
-        if (kSparse && !((list_sel[j] >> t) & 1u)) {
-          // Not kept for this query tile: P = 0, running max and sum unchanged.
-          uint32_t z[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) z[i] = 0u;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) tmem_st16(tS + q * 16, z);
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(BAR_PFULL + t));
-          continue;
-        }
         const int kv_tail = kSparse ? (list_tiles[j] == p.sp_nkb - 1 ? p.sp_tail : kBN)
                                     : (j == n_kv1 - 1) ? tail1 : (j == n_kv - 1) ? tail2 : kBN;
         if (kv_tail < kBN) {
@@ -529,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         fadd2(ls[4], ls[5], ls[4], ls[5], ls[6], ls[7]);
         fadd2(ls[0], ls[1], ls[0], ls[1], ls[4], ls[5]);
         l += ls[0] + ls[1];
-        if (j > 0 && __any_sync(0xffffffffu, need)) {
+        if (kept > 0 && __any_sync(0xffffffffu, need)) {
           // O_t holds PV(0..j-1), complete because S_t(j) is (in-order MMAs).
           const float f = alpha;
 #pragma unroll
@@ -546,6 +580,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_PFULL + t));
+        ++kept;
+      }
+      // A tile whose list keeps nothing has no O (TMEM never written): its
+      // valid rows are 0.
+      if (ok && kept == 0) {
+        const int row = qrow0 + t * kBM + (warp & 3) * 32 + lane;
+        if (row < sg.nq) {
+          uint4* dst = reinterpret_cast<uint4*>(
+              p.out + static_cast<int64_t>(sg.q_row0 + row) * p.out_stride + head * kHeadDim);
+          for (int v4 = 0; v4 < 16; ++v4) dst[v4] = make_uint4(0, 0, 0, 0);
+        }
+        ok = false;
       }
       if (ok) ok = wait_warp(bar(BAR_OFINAL + t), 0, wctx, H3_STATUS_TIMEOUT_SOFTMAX);
       if (ok) {

@@ -139,3 +139,58 @@ def test_sol_attention_full_size_sampled():
                                      O.widen(vc[:, h:h + 1]), n, keep[h:h + 1], B, SCALE, rows=rows)
         ref[:, h] = r[:, 0]
     gate(got, ref, "sol attention full size")
+
+
+def _lists_from_mask(keep):
+    """bool [H, nqb, nkb] -> (lists, counts) in the layout block_select writes."""
+    H, nqb, nkb = keep.shape
+    lists = torch.full((H, nqb, nkb), -1, dtype=torch.int32)
+    counts = torch.zeros((H, nqb), dtype=torch.int32)
+    for h in range(H):
+        for a in range(nqb):
+            idx = np.nonzero(keep[h, a])[0]
+            lists[h, a, :idx.size] = torch.from_numpy(idx.astype(np.int32))
+            counts[h, a] = idx.size
+    return lists.cuda(), counts.cuda()
+
+
+# Query tiles are paired per CTA (blocks 2i and 2i + 1): these masks give the
+# two tiles of a pair different, disjoint or empty lists.
+def _mask(kind, H, nb):
+    keep = np.zeros((H, nb, nb), dtype=bool)
+    for a in range(nb):
+        for b in range(nb):
+            if kind == "even_odd":          # tile 0 of a pair: even blocks, tile 1: odd
+                keep[:, a, b] = (b % 2) == (a % 2)
+            elif kind == "one_tile_empty":  # tile 1 of every pair keeps nothing
+                keep[:, a, b] = (a % 2 == 0) and (b % 3 != 1)
+            elif kind == "first_tile_empty":
+                keep[:, a, b] = (a % 2 == 1) and (b >= a // 2)
+            elif kind == "single_shared":   # both tiles keep only the last block
+                keep[:, a, b] = b == nb - 1
+    if kind == "per_head":
+        rng = np.random.default_rng(11)
+        keep = rng.random((H, nb, nb)) < 0.3
+        keep[0, 1::2] = False               # head 0: second tiles empty
+    return keep
+
+
+@pytest.mark.parametrize("kind", ["even_odd", "one_tile_empty", "first_tile_empty",
+                                  "single_shared", "per_head"])
+def test_sparse_attention_tiles_with_different_lists(kind):
+    H, rows = 3, 1000                        # 8 blocks, the last one partial (104 rows)
+    nb = -(-rows // B)
+    q, k, v = inputs(H, rows, seed=21)
+    keep = _mask(kind, H, nb)
+    lists, counts = _lists_from_mask(keep)
+    out = torch.full((rows, H, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    h3.sparse_attention(q, k, v, lists, counts, rows, SCALE, out=out)
+    torch.cuda.synchronize()
+    ref = O.block_sparse_attention(O.widen(q), O.widen(k), O.widen(v), rows, keep, B, SCALE)
+    got = O.widen(out)
+    none = ~keep.any(-1)                     # [H, nqb]: query blocks that keep nothing
+    for h in range(H):
+        for a in range(nb):
+            if none[h, a]:
+                assert (got[a * B:(a + 1) * B, h] == 0).all(), f"head {h} block {a} not zero"
+    gate(got, ref, kind)
