@@ -9,6 +9,7 @@
 // population standard deviation over all KV blocks; "exceed" is strict;
 // a block holding any prefix row is a prefix block.  Arithmetic is fp32 in
 // a fixed order, so the selection is deterministic run to run.
+#include <atomic>
 #include <cmath>
 
 #include "h3_internal.h"
@@ -48,75 +49,77 @@ __global__ void __launch_bounds__(128) block_means_kernel(const __nv_bfloat16* _
 }
 
 constexpr int kSelThreads = 256;
+constexpr int kSelQB = kSelThreads / 32;  // query blocks per CTA: one warp each
 
-// grid (n_q_blocks, n_heads): scores of one query block against every KV
-// block, their mean and population std, and the ordered list of kept blocks.
+// grid (ceil(nqb / kSelQB), n_heads): the scores of kSelQB query blocks
+// against every KV block (each key mean is read once per CTA and dotted with
+// all kSelQB query means), then per query block -- one warp each -- the mean
+// and population std of its scores and the ordered list of kept blocks.
+// Dynamic shared memory: kSelQB x nkb scores.
 __global__ void __launch_bounds__(kSelThreads) block_select_kernel(
     const float* __restrict__ qm, const float* __restrict__ km, int nqb, int nkb, int H,
     float scale, float tau, int n_prefix, float* __restrict__ scores_out,
     int32_t* __restrict__ lists, int32_t* __restrict__ counts) {
-  __shared__ float qv[kHeadDim];
-  __shared__ float sc[kMaxSparseBlocks];
-  __shared__ float red[kSelThreads / 32];
-  __shared__ int warp_base[kSelThreads / 32 + 1];
-  const int a = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  extern __shared__ float sc[];  // [kSelQB][nkb]
+  __shared__ float4 qv[kSelQB][kHeadDim / 4];
+  const int a0 = blockIdx.x * kSelQB, h = blockIdx.y, tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
-  if (tid < kHeadDim) qv[tid] = qm[(static_cast<int64_t>(a) * H + h) * kHeadDim + tid];
+  for (int i = tid; i < kSelQB * kHeadDim / 4; i += kSelThreads) {
+    const int qb = i / (kHeadDim / 4), c4 = i % (kHeadDim / 4);
+    qv[qb][c4] = a0 + qb < nqb
+                     ? __ldg(reinterpret_cast<const float4*>(qm + (static_cast<int64_t>(a0 + qb) * H + h) * kHeadDim) + c4)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   __syncthreads();
   for (int b = tid; b < nkb; b += kSelThreads) {
     const float4* kr = reinterpret_cast<const float4*>(km + (static_cast<int64_t>(b) * H + h) * kHeadDim);
-    float s = 0.f;
-#pragma unroll 8
+    float s[kSelQB];
+#pragma unroll
+    for (int qb = 0; qb < kSelQB; ++qb) s[qb] = 0.f;
+#pragma unroll 4
     for (int c4 = 0; c4 < kHeadDim / 4; ++c4) {
       const float4 kv = __ldg(kr + c4);
-      s = fmaf(qv[4 * c4], kv.x, s);
-      s = fmaf(qv[4 * c4 + 1], kv.y, s);
-      s = fmaf(qv[4 * c4 + 2], kv.z, s);
-      s = fmaf(qv[4 * c4 + 3], kv.w, s);
+#pragma unroll
+      for (int qb = 0; qb < kSelQB; ++qb) {  // channel order fixed: the sum is deterministic
+        const float4 q = qv[qb][c4];
+        s[qb] = fmaf(q.x, kv.x, s[qb]);
+        s[qb] = fmaf(q.y, kv.y, s[qb]);
+        s[qb] = fmaf(q.z, kv.z, s[qb]);
+        s[qb] = fmaf(q.w, kv.w, s[qb]);
+      }
     }
-    sc[b] = s * scale;
+#pragma unroll
+    for (int qb = 0; qb < kSelQB; ++qb) sc[qb * nkb + b] = s[qb] * scale;
   }
   __syncthreads();
+  const int a = a0 + warp;
+  if (a >= nqb) return;
+  const float* row = sc + warp * nkb;
   // mean, then the population variance about it (two passes, fixed order)
-  auto block_sum = [&](float v) -> float {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    float t = 0.f;
-    for (int w = 0; w < kSelThreads / 32; ++w) t += red[w];
-    __syncthreads();
-    return t;
-  };
   float part = 0.f;
-  for (int b = tid; b < nkb; b += kSelThreads) part += sc[b];
-  const float mu = block_sum(part) / static_cast<float>(nkb);
+  for (int b = lane; b < nkb; b += 32) part += row[b];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  const float mu = part / static_cast<float>(nkb);
   part = 0.f;
-  for (int b = tid; b < nkb; b += kSelThreads) part += (sc[b] - mu) * (sc[b] - mu);
-  const float sd = sqrtf(block_sum(part) / static_cast<float>(nkb));
-  const float thr = mu + tau * sd;
+  for (int b = lane; b < nkb; b += 32) part += (row[b] - mu) * (row[b] - mu);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  const float thr = mu + tau * sqrtf(part / static_cast<float>(nkb));
   // ordered compaction of the kept blocks
   int32_t* list = lists + (static_cast<int64_t>(h) * nqb + a) * nkb;
   int base = 0;
-  for (int b0 = 0; b0 < nkb; b0 += kSelThreads) {
-    const int b = b0 + tid;
-    const bool keep = b < nkb && (a < n_prefix || b < n_prefix || sc[b] > thr);
+  for (int b0 = 0; b0 < nkb; b0 += 32) {
+    const int b = b0 + lane;
+    const bool keep = b < nkb && (a < n_prefix || b < n_prefix || row[b] > thr);
     const unsigned m = __ballot_sync(0xffffffffu, keep);
-    if (lane == 0) warp_base[warp + 1] = __popc(m);
-    __syncthreads();
-    if (tid == 0) {
-      warp_base[0] = 0;
-      for (int w = 1; w <= kSelThreads / 32; ++w) warp_base[w] += warp_base[w - 1];
-    }
-    __syncthreads();
-    if (keep) list[base + warp_base[warp] + __popc(m & ((1u << lane) - 1u))] = b;
-    base += warp_base[kSelThreads / 32];
-    __syncthreads();
+    if (keep) list[base + __popc(m & ((1u << lane) - 1u))] = b;
+    base += __popc(m);
   }
-  if (tid == 0) counts[static_cast<int64_t>(h) * nqb + a] = base;
+  if (lane == 0) counts[static_cast<int64_t>(h) * nqb + a] = base;
   if (scores_out != nullptr)
-    for (int b = tid; b < nkb; b += kSelThreads)
-      scores_out[(static_cast<int64_t>(h) * nqb + a) * nkb + b] = sc[b];
+    for (int b = lane; b < nkb; b += 32)
+      scores_out[(static_cast<int64_t>(h) * nqb + a) * nkb + b] = row[b];
 }
 
 }  // namespace
@@ -131,8 +134,20 @@ cudaError_t launch_block_means(const __nv_bfloat16* x, int64_t stride, int64_t n
 cudaError_t launch_block_select(const float* qm, const float* km, int nqb, int nkb, int H,
                                 float scale, float tau, int n_prefix, float* scores,
                                 int32_t* lists, int32_t* counts, cudaStream_t stream) {
-  block_select_kernel<<<dim3(nqb, H), kSelThreads, 0, stream>>>(qm, km, nqb, nkb, H, scale, tau,
-                                                               n_prefix, scores, lists, counts);
+  const size_t smem = static_cast<size_t>(kSelQB) * nkb * sizeof(float);  // <= 64 KB
+  static std::atomic<int> attr_set[64];  // opt-in above 48 KB, once per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (attr_set[dev].load() == 0) {
+    e = cudaFuncSetAttribute(block_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSelQB * kMaxSparseBlocks * sizeof(float)));
+    if (e != cudaSuccess) return e;
+    attr_set[dev].store(1);
+  }
+  block_select_kernel<<<dim3((nqb + kSelQB - 1) / kSelQB, H), kSelThreads, smem, stream>>>(
+      qm, km, nqb, nkb, H, scale, tau, n_prefix, scores, lists, counts);
   return cudaGetLastError();
 }
 
