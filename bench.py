@@ -98,6 +98,20 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def mufu_bound(w, attn_ms, clocks, sms=152, ex2_per_clk_per_sm=32):
+    """Secondary bound of the attention kernel: one ex2 per (valid query,
+    valid key, head) on the MUFU, against 32 lanes per clock per SM (the rate
+    the XU counters imply on this part) at the sampled median SM clock."""
+    ex2 = float(w.n_heads * sum(s.n_valid_q() * s.n_valid_kv() for s in w.segments))
+    mhz = clocks.get("sm_mhz") or clocks.get("sm_max_mhz")
+    if not mhz or attn_ms <= 0:
+        return {"bound": "mufu_ex2", "ex2_per_launch": ex2, "frac": None}
+    peak = sms * ex2_per_clk_per_sm * mhz * 1e6
+    achieved = ex2 / (attn_ms * 1e-3)
+    return {"bound": "mufu_ex2", "ex2_per_launch": ex2, "achieved_per_s": round(achieved, 0),
+            "peak_per_s": round(peak, 0), "frac": round(achieved / peak, 4)}
+
+
 # ------------------------------------------------------- replicas (N > 1)
 def max_over_ranks(values, dist, device):
     """Element-wise maximum of per-rank timings over all ranks: the slowest
@@ -240,6 +254,7 @@ def bench_gpu(args):
     if dist is not None:
         dist.barrier()
     ms_total = t_start.elapsed_time(t_end)
+    clk_summary = clk.summary()
     attn_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
     # The prologue alone (in the step it follows the previous attention,
     # whose last output lines are still being written back from L2).
@@ -365,7 +380,8 @@ def bench_gpu(args):
                      "peak": peak, "unit": "TFLOP/s", "frac": round(attn_tflops / peak, 4),
                      "frac_of_burst": round(attn_tflops / pk["bf16"], 4),
                      "peak_source": f"{pk['source']} bf16 (sustained; burst {pk['bf16']})",
-                     "kernel": "attn_fwd_kernel", "traffic": traffic},
+                     "kernel": "attn_fwd_kernel", "traffic": traffic,
+                     "secondary": mufu_bound(w, attn_ms, clk_summary)},
         "attention_ms": round(attn_ms, 4),
         "attention_tflops": round(attn_tflops, 2),
         "prologue_us": round(pro_ms * 1e3, 2) if pro_ms else None,
@@ -385,7 +401,7 @@ def bench_gpu(args):
                 "path": (f"HostPipeline: {len(pipe.groups)} head groups, copies overlapped with compute"
                          if pipe is not None else "copy in, step, copy out")},
         "gpu_launches": launches_per_step(w) * args.steps,
-        "clocks": clk.summary(),
+        "clocks": clk_summary,
         "parity": dict(parity, passed=True),
         "cpu_baseline": cpu,
     }
