@@ -256,6 +256,7 @@ def bench_gpu(args):
     ms_total = t_start.elapsed_time(t_end)
     clk_summary = clk.summary()
     attn_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
+    step_each = [e[0].elapsed_time(e[2]) for e in evs]  # prologue start -> attention end
     # The prologue alone (in the step it follows the previous attention,
     # whose last output lines are still being written back from L2).
     pro_alone_ms = None
@@ -382,6 +383,8 @@ def bench_gpu(args):
                      "peak_source": f"{pk['source']} bf16 (sustained; burst {pk['bf16']})",
                      "kernel": "attn_fwd_kernel", "traffic": traffic,
                      "secondary": mufu_bound(w, attn_ms, clk_summary)},
+        "step_ms_percentiles": {q: round(float(np.percentile(step_each, int(q[1:]))), 4)
+                                for q in ("p10", "p50", "p90")},
         "attention_ms": round(attn_ms, 4),
         "attention_tflops": round(attn_tflops, 2),
         "prologue_us": round(pro_ms * 1e3, 2) if pro_ms else None,
