@@ -302,23 +302,22 @@ def bench_gpu(args):
     host = {k: (v.cpu().pin_memory() if torch.is_tensor(v) else v) for k, v in
             W.make_inputs(w, device=f"cuda:{local}", seed=W.default_seed(w) + rank).items()}
     out_host = torch.empty_like(host["out"]).pin_memory()
-    names = ["q", "k", "v", "wq", "wk"] + (["pos_thw"] if w.self_attention else [])
+    names = ["q", "k", "v"] + (["wq", "wk", "pos_thw"] if w.self_attention else [])
     h2d = sum(host[n].numel() * host[n].element_size() for n in names)
     d2h = out_host.numel() * out_host.element_size()
 
-    pipe = h3.HostPipeline(w.q_rows, w.n_heads) if w.self_attention else None
+    pipe = h3.HostPipeline(w.q_rows, w.n_heads, kv_rows=w.kv_rows)
 
     def e2e_step():
-        if pipe is not None:
-            # head groups copied in, computed and copied out on overlapping streams
+        # head groups copied in, computed and copied out on overlapping streams
+        if w.self_attention:
             pipe.run(host["q"], host["k"], host["v"], host["wq"], host["wk"], host["pos_thw"],
                      host["cu_seqlens_q"], host["valid_len"], out_host, rot=ROT, scale=SCALE,
                      stream=stream)
-            return
-        for n in names:
-            g[n].copy_(host[n], non_blocking=True)
-        run_step(h3, g, w)
-        out_host.copy_(g["out"], non_blocking=True)
+        else:
+            pipe.run_attention(host["q"], host["k"], host["v"], host["cu_seqlens_q"],
+                               host["cu_seqlens_kv"], host["valid_len"], out_host, scale=SCALE,
+                               stream=stream)
 
     for _ in range(min(args.warmup, 2)):
         e2e_step()
@@ -401,8 +400,7 @@ def bench_gpu(args):
                 "statistic": f"median of {len(e_each)} individually timed steps",
                 "mean_ms_per_step": round(e_mean, 3), "max_ms_per_step": round(max(e_each), 3),
                 "value_at_mean": round(whole_job_value(flops, e_mean, world), 3),
-                "path": (f"HostPipeline: {len(pipe.groups)} head groups, copies overlapped with compute"
-                         if pipe is not None else "copy in, step, copy out")},
+                "path": f"HostPipeline: {len(pipe.groups)} head groups, copies overlapped with compute"},
         "gpu_launches": launches_per_step(w) * args.steps,
         "clocks": clk_summary,
         "parity": dict(parity, passed=True),

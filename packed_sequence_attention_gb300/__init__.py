@@ -363,17 +363,22 @@ class HostPipeline:
     bitwise that of ``attention_block`` on the whole tensors.
 
     The device buffers (Q, K, V, out, weights, positions) are allocated once
-    for ``rows`` x ``n_heads``; host tensors must be pinned and shaped like
-    them.
+    for ``rows`` (query rows; ``kv_rows`` key rows, default the same) x
+    ``n_heads``; host tensors must be pinned and shaped like them.
+    ``run`` is the block step (prologue then attention, self-attention);
+    ``run_attention`` is attention alone over separate query and key extents
+    (grouped query ranges).
     """
 
-    def __init__(self, rows: int, n_heads: int, heads_per_group: int = 6, device=None):
+    def __init__(self, rows: int, n_heads: int, heads_per_group: int = 6, device=None,
+                 kv_rows: Optional[int] = None):
         dev = torch.device(device if device is not None else "cuda")
         bf = torch.bfloat16
-        self.rows, self.n_heads = rows, n_heads
+        kv_rows = rows if kv_rows is None else kv_rows
+        self.rows, self.kv_rows, self.n_heads = rows, kv_rows, n_heads
         self.q = torch.empty((rows, n_heads, HEAD_DIM), dtype=bf, device=dev)
-        self.k = torch.empty_like(self.q)
-        self.v = torch.empty_like(self.q)
+        self.k = torch.empty((kv_rows, n_heads, HEAD_DIM), dtype=bf, device=dev)
+        self.v = torch.empty_like(self.k)
         self.out = torch.empty_like(self.q)
         self.wq = torch.empty((n_heads, HEAD_DIM), dtype=bf, device=dev)
         self.wk = torch.empty_like(self.wq)
@@ -384,6 +389,16 @@ class HostPipeline:
         self.s_out = torch.cuda.Stream(device=dev)
         self.s_comp = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
 
+    def run_attention(self, q, k, v, cu_seqlens_q, cu_seqlens_kv, valid_len, out, scale=None,
+                      stream=None) -> None:
+        """Attention alone from pinned host Q, K, V to the pinned host out,
+        with the same head-group overlap as ``run``; the arguments are those
+        of ``attention``."""
+        def compute(h0, h1, sc):
+            attention(self.q[:, h0:h1], self.k[:, h0:h1], self.v[:, h0:h1], cu_seqlens_q,
+                      cu_seqlens_kv, valid_len, scale, self.out[:, h0:h1], sc)
+        self._pipeline(q, k, v, out, compute, None, stream)
+
     def run(self, q, k, v, wq, wk, pos_thw, cu_seqlens, valid_len, out,
             rot=(32, 48, 48), theta=10000.0, eps=1e-6, scale=None, stream=None) -> None:
         """Queue one block step after the work already on ``stream`` (default:
@@ -391,15 +406,27 @@ class HostPipeline:
         synchronise on it (or an event recorded on it) sees ``out`` filled.
         Q, K, V, weights and positions are read from the host tensors; the
         device copies of Q and K are normalised in place."""
+        def compute(h0, h1, sc):
+            attention_block(self.q[:, h0:h1], self.k[:, h0:h1], self.v[:, h0:h1],
+                            self.wq[h0:h1], self.wk[h0:h1], self.pos, cu_seqlens, valid_len,
+                            rot=rot, theta=theta, eps=eps, scale=scale,
+                            out=self.out[:, h0:h1], stream=sc)
+
+        def small_inputs():
+            self.wq.copy_(wq, non_blocking=True)
+            self.wk.copy_(wk, non_blocking=True)
+            self.pos.copy_(pos_thw, non_blocking=True)
+        self._pipeline(q, k, v, out, compute, small_inputs, stream)
+
+    def _pipeline(self, q, k, v, out, compute, small_inputs, stream):
         cur = stream if stream is not None else torch.cuda.current_stream()
         start = torch.cuda.Event()
         start.record(cur)
         for s in (self.s_in, self.s_out, *self.s_comp):
             s.wait_event(start)
-        with torch.cuda.stream(self.s_in):
-            self.wq.copy_(wq, non_blocking=True)
-            self.wk.copy_(wk, non_blocking=True)
-            self.pos.copy_(pos_thw, non_blocking=True)
+        if small_inputs is not None:
+            with torch.cuda.stream(self.s_in):
+                small_inputs()
         for i, (h0, h1) in enumerate(self.groups):
             for dev_t, host_t in ((self.q, q), (self.k, k), (self.v, v)):
                 copy_2d(dev_t[:, h0:h1], host_t[:, h0:h1], self.s_in)
@@ -407,10 +434,7 @@ class HostPipeline:
             landed.record(self.s_in)
             sc = self.s_comp[i % 2]
             sc.wait_event(landed)
-            attention_block(self.q[:, h0:h1], self.k[:, h0:h1], self.v[:, h0:h1],
-                            self.wq[h0:h1], self.wk[h0:h1], self.pos, cu_seqlens, valid_len,
-                            rot=rot, theta=theta, eps=eps, scale=scale,
-                            out=self.out[:, h0:h1], stream=sc)
+            compute(h0, h1, sc)
             done = torch.cuda.Event()
             done.record(sc)
             self.s_out.wait_event(done)

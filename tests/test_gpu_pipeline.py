@@ -57,3 +57,17 @@ def test_host_pipeline_is_bitwise_the_device_path(wl, group):
         assert torch.equal(out.view(torch.int16), ref.cpu().view(torch.int16))
     # the host inputs are untouched (the prologue works on the device copies)
     assert torch.equal(host["q"].view(torch.int16), g["q"].cpu().view(torch.int16))
+
+
+def test_host_pipeline_attention_only_grouped():
+    w = W.custom("grp", 5, [W.Segment(64, 64), W.Segment(200, 900), W.Segment(333, 1500)],
+                 self_attention=False)
+    g = W.make_inputs(w, device="cuda")
+    ref = h3.attention(g["q"], g["k"], g["v"], g["cu_seqlens_q"], g["cu_seqlens_kv"], None, SCALE)
+    host = {n: g[n].cpu().pin_memory() for n in ("q", "k", "v")}
+    pipe = h3.HostPipeline(w.q_rows, w.n_heads, heads_per_group=2, kv_rows=w.kv_rows)
+    out = torch.full(ref.shape, float("nan"), dtype=torch.bfloat16).pin_memory()
+    pipe.run_attention(host["q"], host["k"], host["v"], g["cu_seqlens_q"], g["cu_seqlens_kv"], None,
+                       out, scale=SCALE)
+    torch.cuda.current_stream().synchronize()
+    assert torch.equal(out.view(torch.int16), ref.cpu().view(torch.int16))
