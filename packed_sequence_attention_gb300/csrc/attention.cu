@@ -61,9 +61,13 @@ constexpr uint32_t kOffV = kOffK + kNS * kTileBytes;
 constexpr uint32_t kOffBar = kOffV + kNS * kTileBytes;
 enum {
   BAR_Q = 0,
-  BAR_KVFULL = 1,  // K and V of a ring stage landed (one barrier: fewer waits for the issuer)
-  BAR_KVEMPTY = BAR_KVFULL + kNS,
-  BAR_SFULL = BAR_KVEMPTY + kNS,
+  // K and V rings have their own barriers: a K stage is released as soon as
+  // the last Q.K^T reading it completes, an iteration before its V stage.
+  BAR_KFULL = 1,
+  BAR_VFULL = BAR_KFULL + kNS,
+  BAR_KEMPTY = BAR_VFULL + kNS,
+  BAR_VEMPTY = BAR_KEMPTY + kNS,
+  BAR_SFULL = BAR_VEMPTY + kNS,
   BAR_PFULL = BAR_SFULL + 2,
   BAR_OFINAL = BAR_PFULL + 2,
   BAR_DRAIN = BAR_OFINAL + 2,
@@ -140,8 +144,7 @@ __device__ __forceinline__ bool should_stop(const WaitCtx& w) {
 }
 
 // Single-thread bounded wait.  False = gave up (or another role did).
-__device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, const WaitCtx& w, uint32_t bit) {
-  if (mbar_try_wait(bar, parity)) return true;
+__device__ __noinline__ bool wait1_slow(uint32_t bar, uint32_t parity, const WaitCtx& w, uint32_t bit) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -156,6 +159,14 @@ __device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, const WaitC
       }
     }
   }
+}
+
+// Single-thread bounded wait.  False = gave up (or another role did).  The
+// spin lives out of line so that the issuing thread's hot path holds one
+// try_wait and one branch.
+__device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, const WaitCtx& w, uint32_t bit) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait1_slow(bar, parity, w, bit);
 }
 
 // Bounded wait that only ends on completion or time (no early stop): used to
@@ -295,8 +306,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   if (threadIdx.x == 0) {
     mbar_init(bar(BAR_Q), 1);
     for (int s = 0; s < kNS; ++s) {
-      mbar_init(bar(BAR_KVFULL + s), 1);
-      mbar_init(bar(BAR_KVEMPTY + s), 1);
+      mbar_init(bar(BAR_KFULL + s), 1);
+      mbar_init(bar(BAR_VFULL + s), 1);
+      mbar_init(bar(BAR_KEMPTY + s), 1);
+      mbar_init(bar(BAR_VEMPTY + s), 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(BAR_SFULL + t), 1);
@@ -340,34 +353,38 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         for (int h = 0; h < 2; ++h)
           tma_load_3d(sbase + kOffQ + t * kTileBytes + h * kHalfBytes, tq, bar(BAR_Q), h * 64,
                       head, qrow0 + t * kBM);
-      int armed[kNS];
-      for (int s = 0; s < kNS; ++s) armed[s] = -1;
+      int armed_k[kNS], armed_v[kNS];
+      for (int s = 0; s < kNS; ++s) armed_k[s] = armed_v[s] = -1;
       bool ok = true;
       for (int j = 0; j < n_kv && ok; ++j) {
         const int s = j % kNS, use = j / kNS;
-        if (j >= kNS) ok = wait1(bar(BAR_KVEMPTY + s), (use - 1) & 1, wctx, H3_STATUS_TIMEOUT_LOAD);
+        if (j >= kNS) ok = wait1(bar(BAR_KEMPTY + s), (use - 1) & 1, wctx, H3_STATUS_TIMEOUT_LOAD);
         if (!ok) break;
         if (p.fault == 1 && j == 1) continue;  // test hook: leave this stage empty
         const bool first = kSparse || j < n_kv1;
         const CUtensorMap* tk = first ? tk1 : tk2;
         const CUtensorMap* tv = first ? tv1 : tv2;
         const int row = (kSparse ? static_cast<int>(list_tiles[j]) : (first ? j : j - n_kv1)) * kBN;
-        mbar_arrive_expect_tx(bar(BAR_KVFULL + s), 2 * kTileBytes);
+        mbar_arrive_expect_tx(bar(BAR_KFULL + s), kTileBytes);
         for (int h = 0; h < 2; ++h)
-          tma_load_3d(sbase + kOffK + s * kTileBytes + h * kHalfBytes, tk, bar(BAR_KVFULL + s),
+          tma_load_3d(sbase + kOffK + s * kTileBytes + h * kHalfBytes, tk, bar(BAR_KFULL + s),
                       h * 64, head, row);
+        armed_k[s] = use;
+        if (j >= kNS) ok = wait1(bar(BAR_VEMPTY + s), (use - 1) & 1, wctx, H3_STATUS_TIMEOUT_LOAD);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(BAR_VFULL + s), kTileBytes);
         for (int h = 0; h < 2; ++h)
-          tma_load_3d(sbase + kOffV + s * kTileBytes + h * kHalfBytes, tv, bar(BAR_KVFULL + s),
+          tma_load_3d(sbase + kOffV + s * kTileBytes + h * kHalfBytes, tv, bar(BAR_VFULL + s),
                       h * 64, head, row);
-        armed[s] = use;
+        armed_v[s] = use;
       }
       if (*abort_flag != 0u) {
         // Let every copy this CTA started land before the CTA exits.
         drain_wait(bar(BAR_Q), 0);
-        for (int s = 0; s < kNS; ++s)
-          if (armed[s] >= 0) {
-            drain_wait(bar(BAR_KVFULL + s), armed[s] & 1);
-          }
+        for (int s = 0; s < kNS; ++s) {
+          if (armed_k[s] >= 0) drain_wait(bar(BAR_KFULL + s), armed_k[s] & 1);
+          if (armed_v[s] >= 0) drain_wait(bar(BAR_VFULL + s), armed_v[s] & 1);
+        }
       }
     }
     __syncwarp();  // lanes 1-31 wait here for lane 0
@@ -397,41 +414,113 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
       };
       bool ok = wait1(bar(BAR_Q), 0, wctx, H3_STATUS_TIMEOUT_MMA) &&
-                wait1(bar(BAR_KVFULL), 0, wctx, H3_STATUS_TIMEOUT_MMA);
+                wait1(bar(BAR_KFULL), 0, wctx, H3_STATUS_TIMEOUT_MMA);
       if constexpr (!kSparse) {
+       if (n_tiles == 2) {
+        // Two query tiles: straight-line steps.  The issuing thread pays tens
+        // of cycles for every branch or dependent scalar op between MMAs while
+        // the MMA queue holds only a few, so a step carries no branch but its
+        // waits; the last step (no next Q.K^T) is peeled off.
+        const uint64_t qa0 = dq0, qa1 = dq0 + (kTileBytes >> 4);
+        const uint64_t kb0 = dk0, kb1 = dk0 + (kTileBytes >> 4);
+        const uint64_t vb0 = dv0, vb1 = dv0 + (kTileBytes >> 4);
+        const uint32_t dS0 = tmem + kColS, dS1 = tmem + kColS + 128;
+        const uint32_t dO0 = tmem + kColO, dO1 = tmem + kColO + 128;
+        auto qk_ = [&](uint32_t dS, uint64_t qa, uint64_t kb) {
+#pragma unroll
+          for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+            mma_ss(dS, qa + off, kb + off, kIdescQK, kk > 0 ? 1u : 0u);
+          }
+        };
+        auto pv_ = [&](uint32_t dO, uint32_t dS, uint64_t vb, uint32_t acc) {
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_ts(dO, dS + kk * 8, vb + ((kk * 2048) >> 4), kIdescPV, acc | (kk > 0 ? 1u : 0u));
+        };
+        if (ok) {
+          tc_fence_after();
+          qk_(dS0, qa0, kb0);
+          mma_commit(bar(BAR_SFULL));
+          qk_(dS1, qa1, kb0);
+          mma_commit(bar(BAR_SFULL + 1));
+          mma_commit(bar(BAR_KEMPTY));
+        }
+        int j = 0;
+        for (; j + 1 < n_kv && ok; ++j) {
+          const uint32_t s = static_cast<uint32_t>(j) & 1u, par = s;
+          const uint64_t vbc = s ? vb1 : vb0, kbn = s ? kb0 : kb1;  // V of this stage, K of the next
+          const uint32_t acc = j > 0 ? 1u : 0u;
+          ok = wait1(bar(BAR_PFULL), par, wctx, H3_STATUS_TIMEOUT_MMA);
+          ok &= wait1(bar(BAR_VFULL + s), (static_cast<uint32_t>(j) >> 1) & 1u, wctx,
+                      H3_STATUS_TIMEOUT_MMA);
+          tc_fence_after();
+          pv_(dO0, dS0, vbc, acc);
+          ok &= wait1(bar(BAR_KFULL + (s ^ 1u)), (static_cast<uint32_t>(j + 1) >> 1) & 1u, wctx,
+                      H3_STATUS_TIMEOUT_MMA);
+          tc_fence_after();
+          qk_(dS0, qa0, kbn);
+          mma_commit(bar(BAR_SFULL));
+          ok &= wait1(bar(BAR_PFULL + 1), par, wctx, H3_STATUS_TIMEOUT_MMA);
+          tc_fence_after();
+          pv_(dO1, dS1, vbc, acc);
+          mma_commit(bar(BAR_VEMPTY + s));
+          qk_(dS1, qa1, kbn);
+          mma_commit(bar(BAR_SFULL + 1));
+          mma_commit(bar(BAR_KEMPTY + (s ^ 1u)));
+        }
+        if (ok) {  // last step
+          const uint32_t s = static_cast<uint32_t>(j) & 1u;
+          const uint64_t vbc = s ? vb1 : vb0;
+          const uint32_t acc = j > 0 ? 1u : 0u;
+          ok = wait1(bar(BAR_PFULL), s, wctx, H3_STATUS_TIMEOUT_MMA);
+          ok &= wait1(bar(BAR_VFULL + s), (static_cast<uint32_t>(j) >> 1) & 1u, wctx,
+                      H3_STATUS_TIMEOUT_MMA);
+          tc_fence_after();
+          pv_(dO0, dS0, vbc, acc);
+          mma_commit(bar(BAR_OFINAL));
+          ok &= wait1(bar(BAR_PFULL + 1), s, wctx, H3_STATUS_TIMEOUT_MMA);
+          tc_fence_after();
+          pv_(dO1, dS1, vbc, acc);
+          mma_commit(bar(BAR_OFINAL + 1));
+        }
+       } else {
         if (ok) {
           tc_fence_after();
           for (int t = 0; t < n_tiles; ++t) {
             qk(t, 0);
             mma_commit(bar(BAR_SFULL + t));
           }
+          mma_commit(bar(BAR_KEMPTY));
         }
-        // One flat loop over (KV step j, query tile t) groups keeps the
-        // issuer's path short and identical for every group: wait for P_t(j),
-        // P_t(j).V(j), then (K/V of step j + 1 landed) Q_t.K(j + 1)^T.  V(j)
-        // landed with K(j), which the previous group already waited for.
+        // One flat loop over (KV step j, query tile t) groups: wait for
+        // P_t(j) (and V(j) for the first tile), P_t(j).V(j), then (K(j + 1)
+        // landed) Q_t.K(j + 1)^T; the last tile releases the V and K stages.
         const int n_groups = n_kv * n_tiles;
         for (int g = 0; g < n_groups && ok; ++g) {
           const int j = n_tiles == 2 ? (g >> 1) : g;
           const int t = g - j * n_tiles;
           const int s = j % kNS, s2 = (j + 1) % kNS, use2 = (j + 1) / kNS;
           ok = wait1(bar(BAR_PFULL + t), j & 1, wctx, H3_STATUS_TIMEOUT_MMA);
+          if (ok && t == 0) ok = wait1(bar(BAR_VFULL + s), (j / kNS) & 1, wctx, H3_STATUS_TIMEOUT_MMA);
           if (!ok) break;
           tc_fence_after();
           pv(t, s, j > 0);
-          if (t == n_tiles - 1) mma_commit(bar(BAR_KVEMPTY + s));
+          if (t == n_tiles - 1) mma_commit(bar(BAR_VEMPTY + s));
           if (j + 1 < n_kv) {
             if (t == 0) {
-              ok = wait1(bar(BAR_KVFULL + s2), use2 & 1, wctx, H3_STATUS_TIMEOUT_MMA);
+              ok = wait1(bar(BAR_KFULL + s2), use2 & 1, wctx, H3_STATUS_TIMEOUT_MMA);
               if (!ok) break;
               tc_fence_after();
             }
             qk(t, s2);
             mma_commit(bar(BAR_SFULL + t));
+            if (t == n_tiles - 1) mma_commit(bar(BAR_KEMPTY + s2));
           } else {
             mma_commit(bar(BAR_OFINAL + t));
           }
         }
+       }
       } else {
         // Block-sparse: the steps walk the union of the two tiles' lists; a
         // tile takes part only in the steps its own list keeps (no MMA for
@@ -445,29 +534,34 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
               qk(t, 0);
               mma_commit(bar(BAR_SFULL + t));
             }
+          mma_commit(bar(BAR_KEMPTY));
         }
         for (int j = 0; j < n_kv && ok; ++j) {
           const int s = j % kNS, s2 = (j + 1) % kNS, use2 = (j + 1) / kNS;
-          const int last = keeps(1, j) ? 1 : 0;  // the last tile that reads stage s
-          bool next_landed = false;
+          const int last = keeps(1, j) ? 1 : 0;  // the last tile that reads V(j)
+          const int last_k = (j + 1 < n_kv && keeps(1, j + 1)) ? 1 : 0;  // last reader of K(j + 1)
+          bool v_landed = false, next_landed = false;
           for (int t = 0; t < n_tiles && ok; ++t) {
             if (keeps(t, j)) {
               ok = wait1(bar(BAR_PFULL + t), kept[t] & 1, wctx, H3_STATUS_TIMEOUT_MMA);
+              if (ok && !v_landed) ok = wait1(bar(BAR_VFULL + s), (j / kNS) & 1, wctx, H3_STATUS_TIMEOUT_MMA);
               if (!ok) break;
+              v_landed = true;
               tc_fence_after();
               pv(t, s, kept[t] > 0);
               ++kept[t];
             }
-            if (t == last) mma_commit(bar(BAR_KVEMPTY + s));
+            if (t == last) mma_commit(bar(BAR_VEMPTY + s));
             if (j + 1 < n_kv && keeps(t, j + 1)) {
               if (!next_landed) {
-                ok = wait1(bar(BAR_KVFULL + s2), use2 & 1, wctx, H3_STATUS_TIMEOUT_MMA);
+                ok = wait1(bar(BAR_KFULL + s2), use2 & 1, wctx, H3_STATUS_TIMEOUT_MMA);
                 if (!ok) break;
                 tc_fence_after();
                 next_landed = true;
               }
               qk(t, s2);
               mma_commit(bar(BAR_SFULL + t));
+              if (t == last_k) mma_commit(bar(BAR_KEMPTY + s2));
             }
           }
         }
