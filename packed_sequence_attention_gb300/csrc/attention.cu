@@ -143,8 +143,11 @@ __device__ __forceinline__ bool should_stop(const WaitCtx& w) {
   return false;
 }
 
-// Single-thread bounded wait.  False = gave up (or another role did).
-__device__ __noinline__ bool wait1_slow(uint32_t bar, uint32_t parity, const WaitCtx& w, uint32_t bit) {
+// Single-thread bounded wait.  False = gave up (or another role did).  Kept
+// inline: as a call, the register saves and reloads around it cost the
+// issuing thread more than the spin itself.
+__device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, const WaitCtx& w, uint32_t bit) {
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -159,14 +162,6 @@ __device__ __noinline__ bool wait1_slow(uint32_t bar, uint32_t parity, const Wai
       }
     }
   }
-}
-
-// Single-thread bounded wait.  False = gave up (or another role did).  The
-// spin lives out of line so that the issuing thread's hot path holds one
-// try_wait and one branch.
-__device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, const WaitCtx& w, uint32_t bit) {
-  if (mbar_try_wait(bar, parity)) return true;
-  return wait1_slow(bar, parity, w, bit);
 }
 
 // Bounded wait that only ends on completion or time (no early stop): used to
@@ -415,29 +410,55 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       };
       bool ok = wait1(bar(BAR_Q), 0, wctx, H3_STATUS_TIMEOUT_MMA) &&
                 wait1(bar(BAR_KFULL), 0, wctx, H3_STATUS_TIMEOUT_MMA);
+      // Straight-line pieces for two query tiles.  The issuing thread pays
+      // tens of cycles for every branch or dependent scalar op between MMAs
+      // while the MMA queue holds only a few, so a two-tile step carries no
+      // branch but its waits.
+      const uint64_t qa0 = dq0, qa1 = dq0 + (kTileBytes >> 4);
+      const uint64_t kb0 = dk0, kb1 = dk0 + (kTileBytes >> 4);
+      const uint64_t vb0 = dv0, vb1 = dv0 + (kTileBytes >> 4);
+      const uint32_t dS0 = tmem + kColS, dS1 = tmem + kColS + 128;
+      const uint32_t dO0 = tmem + kColO, dO1 = tmem + kColO + 128;
+      auto qk_ = [&](uint32_t dS, uint64_t qa, uint64_t kb) {
+#pragma unroll
+        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+          mma_ss(dS, qa + off, kb + off, kIdescQK, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto pv_ = [&](uint32_t dO, uint32_t dS, uint64_t vb, uint32_t acc) {
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts(dO, dS + kk * 8, vb + ((kk * 2048) >> 4), kIdescPV, acc | (kk > 0 ? 1u : 0u));
+      };
+      // One step in which both tiles read V(j) and K(j + 1): P_0.V, Q_0.K^T,
+      // P_1.V, release V(j), Q_1.K^T, release K(j + 1).  pp0/pp1: the tiles'
+      // P phases; acc0/acc1: whether their O already holds a partial sum.
+      auto step2 = [&](int j, uint32_t pp0, uint32_t pp1, uint32_t acc0, uint32_t acc1) -> bool {
+        const uint32_t s = static_cast<uint32_t>(j) & 1u;
+        const uint64_t vbc = s ? vb1 : vb0, kbn = s ? kb0 : kb1;  // V of this stage, K of the next
+        bool r = wait1(bar(BAR_PFULL), pp0, wctx, H3_STATUS_TIMEOUT_MMA);
+        r &= wait1(bar(BAR_VFULL + s), (static_cast<uint32_t>(j) >> 1) & 1u, wctx,
+                   H3_STATUS_TIMEOUT_MMA);
+        tc_fence_after();
+        pv_(dO0, dS0, vbc, acc0);
+        r &= wait1(bar(BAR_KFULL + (s ^ 1u)), (static_cast<uint32_t>(j + 1) >> 1) & 1u, wctx,
+                   H3_STATUS_TIMEOUT_MMA);
+        tc_fence_after();
+        qk_(dS0, qa0, kbn);
+        mma_commit(bar(BAR_SFULL));
+        r &= wait1(bar(BAR_PFULL + 1), pp1, wctx, H3_STATUS_TIMEOUT_MMA);
+        tc_fence_after();
+        pv_(dO1, dS1, vbc, acc1);
+        mma_commit(bar(BAR_VEMPTY + s));
+        qk_(dS1, qa1, kbn);
+        mma_commit(bar(BAR_SFULL + 1));
+        mma_commit(bar(BAR_KEMPTY + (s ^ 1u)));
+        return r;
+      };
       if constexpr (!kSparse) {
        if (n_tiles == 2) {
-        // Two query tiles: straight-line steps.  The issuing thread pays tens
-        // of cycles for every branch or dependent scalar op between MMAs while
-        // the MMA queue holds only a few, so a step carries no branch but its
-        // waits; the last step (no next Q.K^T) is peeled off.
-        const uint64_t qa0 = dq0, qa1 = dq0 + (kTileBytes >> 4);
-        const uint64_t kb0 = dk0, kb1 = dk0 + (kTileBytes >> 4);
-        const uint64_t vb0 = dv0, vb1 = dv0 + (kTileBytes >> 4);
-        const uint32_t dS0 = tmem + kColS, dS1 = tmem + kColS + 128;
-        const uint32_t dO0 = tmem + kColO, dO1 = tmem + kColO + 128;
-        auto qk_ = [&](uint32_t dS, uint64_t qa, uint64_t kb) {
-#pragma unroll
-          for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-            const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
-            mma_ss(dS, qa + off, kb + off, kIdescQK, kk > 0 ? 1u : 0u);
-          }
-        };
-        auto pv_ = [&](uint32_t dO, uint32_t dS, uint64_t vb, uint32_t acc) {
-#pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk)
-            mma_ts(dO, dS + kk * 8, vb + ((kk * 2048) >> 4), kIdescPV, acc | (kk > 0 ? 1u : 0u));
-        };
+        // The last step (no next Q.K^T) is peeled off.
         if (ok) {
           tc_fence_after();
           qk_(dS0, qa0, kb0);
@@ -448,26 +469,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
         int j = 0;
         for (; j + 1 < n_kv && ok; ++j) {
-          const uint32_t s = static_cast<uint32_t>(j) & 1u, par = s;
-          const uint64_t vbc = s ? vb1 : vb0, kbn = s ? kb0 : kb1;  // V of this stage, K of the next
-          const uint32_t acc = j > 0 ? 1u : 0u;
-          ok = wait1(bar(BAR_PFULL), par, wctx, H3_STATUS_TIMEOUT_MMA);
-          ok &= wait1(bar(BAR_VFULL + s), (static_cast<uint32_t>(j) >> 1) & 1u, wctx,
-                      H3_STATUS_TIMEOUT_MMA);
-          tc_fence_after();
-          pv_(dO0, dS0, vbc, acc);
-          ok &= wait1(bar(BAR_KFULL + (s ^ 1u)), (static_cast<uint32_t>(j + 1) >> 1) & 1u, wctx,
-                      H3_STATUS_TIMEOUT_MMA);
-          tc_fence_after();
-          qk_(dS0, qa0, kbn);
-          mma_commit(bar(BAR_SFULL));
-          ok &= wait1(bar(BAR_PFULL + 1), par, wctx, H3_STATUS_TIMEOUT_MMA);
-          tc_fence_after();
-          pv_(dO1, dS1, vbc, acc);
-          mma_commit(bar(BAR_VEMPTY + s));
-          qk_(dS1, qa1, kbn);
-          mma_commit(bar(BAR_SFULL + 1));
-          mma_commit(bar(BAR_KEMPTY + (s ^ 1u)));
+          const uint32_t par = static_cast<uint32_t>(j) & 1u;
+          ok = step2(j, par, par, j > 0 ? 1u : 0u, j > 0 ? 1u : 0u);
         }
         if (ok) {  // last step
           const uint32_t s = static_cast<uint32_t>(j) & 1u;
@@ -524,25 +527,36 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       } else {
         // Block-sparse: the steps walk the union of the two tiles' lists; a
         // tile takes part only in the steps its own list keeps (no MMA for
-        // the others).  Its S/P barrier phases count its kept steps.
-        auto keeps = [&](int t, int j) -> bool { return t < n_tiles && ((list_sel[j] >> t) & 1u); };
+        // the others).  Its S/P barrier phases count its kept steps.  sel
+        // bit t: tile t keeps the step (bit 1 is never set for one tile).
         int kept[2] = {0, 0};
+        uint32_t sel = list_sel[0];
         if (ok) {
           tc_fence_after();
-          for (int t = 0; t < n_tiles; ++t)
-            if (keeps(t, 0)) {
+          for (int t = 0; t < 2; ++t)
+            if ((sel >> t) & 1u) {
               qk(t, 0);
               mma_commit(bar(BAR_SFULL + t));
             }
           mma_commit(bar(BAR_KEMPTY));
         }
         for (int j = 0; j < n_kv && ok; ++j) {
+          const uint32_t seln = j + 1 < n_kv ? static_cast<uint32_t>(list_sel[j + 1]) : 0u;
+          if ((sel & seln) == 3u) {
+            // Both tiles read V(j) and K(j + 1): the straight-line step.
+            ok = step2(j, static_cast<uint32_t>(kept[0]) & 1u, static_cast<uint32_t>(kept[1]) & 1u,
+                       kept[0] > 0 ? 1u : 0u, kept[1] > 0 ? 1u : 0u);
+            ++kept[0];
+            ++kept[1];
+            sel = seln;
+            continue;
+          }
           const int s = j % kNS, s2 = (j + 1) % kNS, use2 = (j + 1) / kNS;
-          const int last = keeps(1, j) ? 1 : 0;  // the last tile that reads V(j)
-          const int last_k = (j + 1 < n_kv && keeps(1, j + 1)) ? 1 : 0;  // last reader of K(j + 1)
+          const int last = (sel >> 1) & 1u;    // the last tile that reads V(j)
+          const int last_k = (seln >> 1) & 1u;  // the last tile that reads K(j + 1)
           bool v_landed = false, next_landed = false;
-          for (int t = 0; t < n_tiles && ok; ++t) {
-            if (keeps(t, j)) {
+          for (int t = 0; t < 2 && ok; ++t) {
+            if ((sel >> t) & 1u) {
               ok = wait1(bar(BAR_PFULL + t), kept[t] & 1, wctx, H3_STATUS_TIMEOUT_MMA);
               if (ok && !v_landed) ok = wait1(bar(BAR_VFULL + s), (j / kNS) & 1, wctx, H3_STATUS_TIMEOUT_MMA);
               if (!ok) break;
@@ -552,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
               ++kept[t];
             }
             if (t == last) mma_commit(bar(BAR_VEMPTY + s));
-            if (j + 1 < n_kv && keeps(t, j + 1)) {
+            if ((seln >> t) & 1u) {
               if (!next_landed) {
                 ok = wait1(bar(BAR_KFULL + s2), use2 & 1, wctx, H3_STATUS_TIMEOUT_MMA);
                 if (!ok) break;
@@ -564,6 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
               if (t == last_k) mma_commit(bar(BAR_KEMPTY + s2));
             }
           }
+          sel = seln;
         }
         if (ok)
           for (int t = 0; t < n_tiles; ++t)
