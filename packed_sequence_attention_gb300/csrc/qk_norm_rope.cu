@@ -6,24 +6,27 @@
 // RoPE.  The point of the fusion is to read each wide activation once and
 // write it once, so the kernel is built around keeping HBM busy:
 //
-// * Persistent CTAs of 128 threads walk items g = blockIdx.x + i * gridDim.x;
-//   item g is row g / 2 of Q (g even) or of K (g odd): n_heads * 256
-//   contiguous bytes.
-// * Thread 0 streams items into a 2-stage shared-memory ring with 1-D bulk
-//   async copies (cp.async.bulk, completion on an mbarrier): one item is in
-//   flight while the other is processed.  Small CTAs with a shallow ring let
-//   ~10 CTAs share an SM; on GB300 that beat deeper rings with fewer CTAs
-//   (58,758-row workload: 418 us vs 422 us for whole-row items with 128
-//   threads, 440 us with 256 threads, 444-569 us with 3-4 stages).
-// * Per item, threads 0..63 compute the (cos, sin) of the 64 channel pairs
-//   once into a per-stage table when the item's copy is issued (its position
-//   is fetched one ring-depth ahead); every head of the item reuses them.
+// * Persistent CTAs walk items g = blockIdx.x + i * gridDim.x; item g is row
+//   g / 2 of Q (g even) or of K (g odd): n_heads * 256 contiguous bytes.
+// * Warp roles.  One streaming warp copies items into a 3-stage shared-memory
+//   ring with 1-D bulk async copies (cp.async.bulk, completion on a "full"
+//   mbarrier) and fills each stage's (cos, sin) table for the item's
+//   position; four compute warps consume the stages and give each one back
+//   through an "empty" mbarrier.  No block-wide barrier is left in the loop,
+//   so a compute warp never waits for a slower one.  On the 58,758-row
+//   workload this runs at 401 us against 412 us for the same arithmetic with
+//   all threads computing and a block barrier per item; 2 or 4 stages, or
+//   7 CTAs per SM, were no faster.
+// * Per item, the streaming warp computes the (cos, sin) of the 64 channel
+//   pairs once (two pairs per lane, positions fetched one item ahead); every
+//   head of the item reuses them.
 // * A head-vector (128 channels) is handled by 8 lanes, each owning channel
 //   chunks [8s, 8s+8) and [64+8s, 64+8s+8); the sum of squares is reduced with
 //   three xor-shuffles; results are rounded once to bf16 (RNE) and stored
 //   straight to global memory with 16-byte streaming stores.
 // * Every mbarrier wait is bounded; a wait that gives up sets a bit in the
-//   device status word and the CTA stops.
+//   device status word and the role stops (the streaming warp first lets its
+//   copies in flight land).
 #include <cmath>
 #include <mutex>
 
@@ -35,9 +38,11 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 128;
+constexpr int kComputeWarps = 4;
+constexpr int kThreads = 32 * (kComputeWarps + 1);
 constexpr int kMaxStages = 4;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr size_t kMaxSmemPerBlock = 227 * 1024;  // opt-in dynamic shared memory per CTA
 
 struct NormRopeParams {
   __nv_bfloat16* x[2];
@@ -84,88 +89,119 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 // kLora: the item is base + delta; the sum is rounded to bf16 first, as the
 // separate branches would store it (Sol-H3 section 3.5, precision-preserving
 // LoRA fusion), then normalised and rotated.
+//
+// Warp roles: warps 0..3 compute, warp 4 streams.  The streaming warp waits
+// until every compute warp has released a stage, copies the next row into
+// it and fills the stage's (cos, sin) table; compute warps never wait for
+// one another.
 template <bool kLora>
 __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_constant__ NormRopeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x;
+  const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int sub = lane & 7;                       // channel chunk of this lane
-  const int slot = (tid >> 5) * 4 + (lane >> 3);  // which head-unit of a pass
-  constexpr int kSlots = kThreads / 8;
   const int H = p.n_heads;
   const uint32_t row_bytes = static_cast<uint32_t>(H) * kHeadDim * 2;
   const uint32_t stage_bytes = (kLora ? 2 : 1) * row_bytes;  // one tensor row (+ its delta row)
   const int NST = p.n_stages;
   const uint32_t sbase = smem_u32(smem);
   float2* tab = reinterpret_cast<float2*>(smem + NST * stage_bytes);  // [NST][64] (cos, sin)
-  const uint32_t s_bar = sbase + NST * stage_bytes + NST * 64 * 8;   // mbarriers [NST]
+  const uint32_t full_bar = sbase + NST * stage_bytes + NST * 64 * 8;  // mbarriers [NST]
+  const uint32_t empty_bar = full_bar + 8 * kMaxStages;                // mbarriers [NST]
 
   const int64_t first = blockIdx.x;
   const int64_t step = gridDim.x;
   const int64_t n_items = 2 * p.n_rows;  // item g: row g >> 1, tensor g & 1
   const int64_t n_mine = first < n_items ? (n_items - 1 - first) / step + 1 : 0;
-  const int my_axis = tid < 64 ? p.axis[tid] : -1;
-  const float my_freq = tid < 64 ? p.inv_freq[tid] : 0.0f;
-
-  // Position of row i of this CTA along this thread's pair axis (threads < 64).
-  auto load_pos = [&](int64_t i) -> int32_t {
-    if (my_axis < 0 || i >= n_mine) return 0;
-    return __ldg(p.pos + ((first + i * step) >> 1) * 3 + my_axis);
-  };
-  auto fill_table = [&](int s, int32_t pos) {
-    if (tid < 64) {
-      float c = 1.0f, sn = 0.0f;
-      if (my_axis >= 0) sincosf(static_cast<float>(pos) * my_freq, &sn, &c);
-      tab[s * 64 + tid] = make_float2(c, sn);
-    }
-  };
-  auto issue = [&](int64_t i) {  // bytes of row i of this CTA -> stage i % NST
-    const int s = static_cast<int>(i % NST);
-    const int64_t g = first + i * step;
-    const int64_t row = g >> 1;
-    const int tt = static_cast<int>(g & 1);
-    const uint32_t bar = s_bar + 8 * s;
-    mbar_arrive_expect_tx(bar, stage_bytes);
-    bulk_load(sbase + s * stage_bytes, p.x[tt] + row * p.stride[tt], row_bytes, bar);
-    if (kLora)
-      bulk_load(sbase + s * stage_bytes + row_bytes, p.d[tt] + row * p.dstride[tt], row_bytes, bar);
-  };
 
   if (tid == 0) {
-    for (int s = 0; s < NST; ++s) mbar_init(s_bar + 8 * s, 1);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(full_bar + 8 * s, 1 + 32);            // the copy's arrive + one per table lane
+      mbar_init(empty_bar + 8 * s, kComputeWarps);  // one per compute warp
+    }
     fence_mbar_init();
-    for (int64_t i = 0; i < n_mine && i < NST; ++i) issue(i);
   }
-  for (int64_t i = 0; i < n_mine && i < NST; ++i) fill_table(static_cast<int>(i), load_pos(i));
   __syncthreads();
 
+  // Bounded wait; false = gave up.
+  auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    return true;
+  };
+
+  if (warp == kComputeWarps) {
+    // ------------------------------------------------------------ streaming
+    const int ax0 = p.axis[lane], ax1 = p.axis[lane + 32];
+    const float f0 = p.inv_freq[lane], f1 = p.inv_freq[lane + 32];
+    auto pos_of = [&](int64_t i, int ax) -> int32_t {
+      if (ax < 0 || i >= n_mine) return 0;
+      return __ldg(p.pos + ((first + i * step) >> 1) * 3 + ax);
+    };
+    int32_t pn0 = pos_of(0, ax0), pn1 = pos_of(0, ax1);
+    int64_t i = 0;
+    bool ok = true;
+    for (; i < n_mine; ++i) {
+      const int s = static_cast<int>(i % NST);
+      if (i >= NST) {
+        const uint32_t par = static_cast<uint32_t>((i / NST - 1) & 1);
+        bool w = true;
+        if (lane == 0) w = wait(empty_bar + 8 * s, par);
+        if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) {
+          ok = false;
+          break;
+        }
+      }
+      const uint32_t bar = full_bar + 8 * s;
+      if (lane == 0) {
+        const int64_t g = first + i * step;
+        const int64_t row = g >> 1;
+        const int tt = static_cast<int>(g & 1);
+        mbar_arrive_expect_tx(bar, stage_bytes);
+        bulk_load(sbase + s * stage_bytes, p.x[tt] + row * p.stride[tt], row_bytes, bar);
+        if (kLora)
+          bulk_load(sbase + s * stage_bytes + row_bytes, p.d[tt] + row * p.dstride[tt], row_bytes, bar);
+      }
+      const int32_t q0 = pn0, q1 = pn1;
+      pn0 = pos_of(i + 1, ax0);  // next row's positions, in flight meanwhile
+      pn1 = pos_of(i + 1, ax1);
+      float c0 = 1.0f, s0 = 0.0f, c1 = 1.0f, s1 = 0.0f;
+      if (ax0 >= 0) sincosf(static_cast<float>(q0) * f0, &s0, &c0);
+      if (ax1 >= 0) sincosf(static_cast<float>(q1) * f1, &s1, &c1);
+      tab[s * 64 + lane] = make_float2(c0, s0);
+      tab[s * 64 + lane + 32] = make_float2(c1, s1);
+      mbar_arrive(bar);
+    }
+    if (lane == 0) {
+      if (!ok) atomicOr(p.status, H3_STATUS_TIMEOUT_PROLOGUE);
+      // Let every copy this CTA started land before it exits (bounded): the
+      // last NST issued rows.
+      for (int64_t j = (i > NST ? i - NST : 0); j < i; ++j)
+        wait(full_bar + 8 * (j % NST), static_cast<uint32_t>((j / NST) & 1));
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- compute
+  const int sub = lane & 7;                 // channel chunk of this lane
+  const int slot = warp * 4 + (lane >> 3);  // which head-unit of a pass
+  constexpr int kSlots = kComputeWarps * 4;
   const int n_units = H;
   for (int64_t i = 0; i < n_mine; ++i) {
     const int s = static_cast<int>(i % NST);
     const uint32_t parity = static_cast<uint32_t>((i / NST) & 1);
     const int64_t row = (first + i * step) >> 1;
     const int tsel = static_cast<int>((first + i * step) & 1);
-    const int32_t pos_ahead = load_pos(i + NST);  // in flight while this row is processed
-
-    // Wait for this row's bytes (bounded).
-    bool ok = mbar_try_wait(s_bar + 8 * s, parity);
-    if (!ok) {
-      const uint64_t t0 = globaltimer_ns();
-      while (!(ok = mbar_try_wait(s_bar + 8 * s, parity))) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+    // Wait for this row's bytes and table (bounded; uniform across the warp).
+    bool ok = mbar_try_wait(full_bar + 8 * s, parity);
+    if (!__all_sync(0xffffffffu, ok)) {
+      ok = wait(full_bar + 8 * s, parity);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) atomicOr(p.status, H3_STATUS_TIMEOUT_PROLOGUE);
+        return;
       }
-    }
-    if (__syncthreads_or(!ok)) {
-      if (tid == 0) {
-        atomicOr(p.status, H3_STATUS_TIMEOUT_PROLOGUE);
-        // Let the copies this CTA started land before it exits (bounded).
-        for (int64_t j = i; j < n_mine && j < i + NST; ++j) {
-          const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(s_bar + 8 * (j % NST), static_cast<uint32_t>((j / NST) & 1)))
-            if (globaltimer_ns() - t0 > kWaitLimitNs) break;
-        }
-      }
-      return;
     }
     float cs[8], sn[8];
 #pragma unroll
@@ -228,20 +264,17 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_con
       __stcs(dst + sub, make_uint4(o[0], o[1], o[2], o[3]));
       __stcs(dst + 8 + sub, make_uint4(o[4], o[5], o[6], o[7]));
     }
-    __syncthreads();  // stage s and table s are free again
-    if (i + NST < n_mine) {
-      if (tid == 0) issue(i + NST);
-      fill_table(s, pos_ahead);
-    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_bar + 8 * s);  // this warp is done with stage s
   }
 }
 
 }  // namespace
 
 int prologue_max_heads(bool lora) {
-  // Two stages of one tensor row (256 B per head; twice that with the LoRA
-  // delta row) plus two cos/sin tables and the barriers must fit in 227 KB of
-  // shared memory: 452 heads (225 with LoRA); keep 448 (220).
+  // At least two stages of one tensor row (256 B per head; twice that with
+  // the LoRA delta row) plus two cos/sin tables and the barriers must fit in
+  // 227 KB of shared memory: 452 heads (225 with LoRA); keep 448 (220).
   return lora ? 220 : 448;
 }
 
@@ -280,16 +313,18 @@ cudaError_t launch_qk_norm_rope(const NormRopeArgs& a, cudaStream_t stream) {
       p.inv_freq[pair] = 0.0f;
     }
   }
-  // Ring depth: two stages (one item in flight while one is processed).
+  // Ring depth: three stages where they fit in shared memory, else two
+  // (very wide rows).
   const bool lora = a.dq != nullptr;
   p.d[0] = a.dq;
   p.d[1] = a.dk;
   p.dstride[0] = a.dq_stride;
   p.dstride[1] = a.dk_stride;
   const size_t stage_bytes = (lora ? 2ull : 1ull) * a.n_heads * kHeadDim * 2;
-  const int nst = 2;
+  auto smem_for = [&](int nst) { return nst * (stage_bytes + 64 * 8) + 2 * kMaxStages * 8; };
+  const int nst = smem_for(3) <= kMaxSmemPerBlock ? 3 : 2;
   p.n_stages = nst;
-  const size_t smem = nst * (stage_bytes + 64 * 8) + kMaxStages * 8;
+  const size_t smem = smem_for(nst);
   auto kernel = lora ? qk_norm_rope_kernel<true> : qk_norm_rope_kernel<false>;
   // The attribute only ever grows, so a launch never runs under a smaller
   // limit that another thread set after it checked.
