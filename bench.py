@@ -197,6 +197,9 @@ def cpu_baseline(O, inp_cpu, w, n_heads_sample, n_rows_sample):
     flops = 4.0 * 128 * nkv * len(rows) * n_heads_sample
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
             "kind": "oracle",
+            "ms_per_query_row_head": round(dt / (len(rows) * n_heads_sample) * 1e3, 3),
+            # the whole workload at the sample's rate (not run)
+            "extrapolated_full_s": round(w.attention_flops() / (flops / dt), 1),
             "sample": f"{len(rows)} query rows x {n_heads_sample} heads of '{w.name}' against "
                       f"all {nkv} valid keys (fp64 NumPy oracle incl. the K prologue), "
                       f"{dt:.1f} s wall"}
