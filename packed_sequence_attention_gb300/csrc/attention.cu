@@ -270,29 +270,67 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
       }
       __syncwarp();
-      int base = 0;
+      // Step order: blocks both tiles keep (B), then the two tiles' own
+      // blocks alternating (E0, E1, E0, ...), then the rest of the longer
+      // one.  The online softmax does not depend on the order of the keys;
+      // this one gives the issuer work from both tiles at every step while
+      // both have any, so the tiles' Q.K^T -> softmax -> P.V chains overlap.
+      int nb = 0, n0 = 0, n1 = 0;
+      for (int w = lane; w < nwords; w += 32) {
+        const uint32_t b0 = bits[w], b1 = bits[kListWords + w];
+        nb += __popc(b0 & b1);
+        n0 += __popc(b0 & ~b1);
+        n1 += __popc(b1 & ~b0);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        nb += __shfl_xor_sync(0xffffffffu, nb, o);
+        n0 += __shfl_xor_sync(0xffffffffu, n0, o);
+        n1 += __shfl_xor_sync(0xffffffffu, n1, o);
+      }
+      const int m = n0 < n1 ? n0 : n1;
+      int rb = 0, r0 = 0, r1 = 0;  // ranks before this group of 32 words
       for (int w0 = 0; w0 < nwords; w0 += 32) {
         const int w = w0 + lane;
         const uint32_t b0 = w < nwords ? bits[w] : 0u;
         const uint32_t b1 = w < nwords ? bits[kListWords + w] : 0u;
-        uint32_t u = b0 | b1;
-        const int n = __popc(u);
-        int incl = n;
+        const int cb = __popc(b0 & b1), c0 = __popc(b0 & ~b1), c1 = __popc(b1 & ~b0);
+        int ib = cb, i0 = c0, i1 = c1;  // inclusive scans over the lanes
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
+          const int yb = __shfl_up_sync(0xffffffffu, ib, o);
+          const int y0 = __shfl_up_sync(0xffffffffu, i0, o);
+          const int y1 = __shfl_up_sync(0xffffffffu, i1, o);
+          if (lane >= o) {
+            ib += yb;
+            i0 += y0;
+            i1 += y1;
+          }
         }
-        int pos = base + incl - n;
+        int kb = rb + ib - cb, k0 = r0 + i0 - c0, k1 = r1 + i1 - c1;
+        uint32_t u = b0 | b1;
         while (u) {
           const int bit = __ffs(u) - 1;
           u &= u - 1;
+          const uint32_t sl = ((b0 >> bit) & 1u) | (((b1 >> bit) & 1u) << 1);
+          int pos;
+          if (sl == 3u) {
+            pos = kb++;
+          } else if (sl == 1u) {
+            pos = nb + (k0 < m ? 2 * k0 : m + k0);
+            ++k0;
+          } else {
+            pos = nb + (k1 < m ? 2 * k1 + 1 : m + k1);
+            ++k1;
+          }
           tiles[pos] = static_cast<uint16_t>(w * 32 + bit);
-          sel[pos] = static_cast<uint8_t>(((b0 >> bit) & 1u) | (((b1 >> bit) & 1u) << 1));
-          ++pos;
+          sel[pos] = static_cast<uint8_t>(sl);
         }
-        base += __shfl_sync(0xffffffffu, incl, 31);
+        rb += __shfl_sync(0xffffffffu, ib, 31);
+        r0 += __shfl_sync(0xffffffffu, i0, 31);
+        r1 += __shfl_sync(0xffffffffu, i1, 31);
       }
+      const int base = nb + n0 + n1;
       if (lane == 0) *reinterpret_cast<volatile int*>(gbase + kOffList) = base;
     }
   }
@@ -527,20 +565,43 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       } else {
         // Block-sparse: the steps walk the union of the two tiles' lists; a
         // tile takes part only in the steps its own list keeps (no MMA for
-        // the others).  Its S/P barrier phases count its kept steps.  sel
-        // bit t: tile t keeps the step (bit 1 is never set for one tile).
+        // the others), and its S/P barrier phases count its kept steps.
+        // sel bit t: tile t keeps the step (bit 1 is never set for one tile).
+        //
+        // Each tile's next Q.K^T is issued as soon as (a) its previous P.V is
+        // issued (P aliases S) and (b) the K block is within the ring's reach:
+        // at step j the ring can hold K(j + 1) and K(j + 2), because every
+        // Q.K^T of step j was issued before step j.  Q_t.K(n)^T is thus issued
+        // by step n - 1 at the latest, and the tiles' chains interleave.
         int kept[2] = {0, 0};
-        uint32_t sel = list_sel[0];
-        if (ok) {
+        int nxt[2];         // tile t's next kept step whose Q.K^T is not issued (n_kv: none)
+        bool sfree[2] = {true, true};  // tile t's S/P columns may take a new Q.K^T
+        auto next_kept = [&](int t, int from) -> int {
+          int n = from;
+          while (n < n_kv && !((list_sel[n] >> t) & 1u)) ++n;
+          return n;
+        };
+        nxt[0] = next_kept(0, 0);
+        nxt[1] = next_kept(1, 0);
+        // Q_t.K(nxt[t])^T if allowed with the ring reaching step `reach`.
+        auto issue_qk = [&](int t, int reach) -> bool {
+          const int n = nxt[t];
+          if (!sfree[t] || n >= n_kv || n > reach) return true;
+          const int sn = n % kNS;
+          if (!wait1(bar(BAR_KFULL + sn), (n / kNS) & 1, wctx, H3_STATUS_TIMEOUT_MMA)) return false;
           tc_fence_after();
-          for (int t = 0; t < 2; ++t)
-            if ((sel >> t) & 1u) {
-              qk(t, 0);
-              mma_commit(bar(BAR_SFULL + t));
-            }
-          mma_commit(bar(BAR_KEMPTY));
-        }
+          qk(t, sn);
+          mma_commit(bar(BAR_SFULL + t));
+          sfree[t] = false;
+          nxt[t] = next_kept(t, n + 1);
+          // The last reader of K(n) releases its stage.
+          const int o = t ^ 1;
+          if (!((list_sel[n] >> o) & 1u) || nxt[o] > n) mma_commit(bar(BAR_KEMPTY + sn));
+          return true;
+        };
+        if (ok) ok = issue_qk(0, kNS - 1) && issue_qk(1, kNS - 1);
         for (int j = 0; j < n_kv && ok; ++j) {
+          const uint32_t sel = list_sel[j];
           const uint32_t seln = j + 1 < n_kv ? static_cast<uint32_t>(list_sel[j + 1]) : 0u;
           if ((sel & seln) == 3u) {
             // Both tiles read V(j) and K(j + 1): the straight-line step.
@@ -548,37 +609,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                        kept[0] > 0 ? 1u : 0u, kept[1] > 0 ? 1u : 0u);
             ++kept[0];
             ++kept[1];
-            sel = seln;
+            nxt[0] = next_kept(0, j + 2);
+            nxt[1] = next_kept(1, j + 2);
             continue;
           }
-          const int s = j % kNS, s2 = (j + 1) % kNS, use2 = (j + 1) / kNS;
-          const int last = (sel >> 1) & 1u;    // the last tile that reads V(j)
-          const int last_k = (seln >> 1) & 1u;  // the last tile that reads K(j + 1)
-          bool v_landed = false, next_landed = false;
+          const int s = j % kNS;
+          // A tile idle at this step: its next Q.K^T may have come in reach.
+          for (int t = 0; t < 2 && ok; ++t)
+            if (!((sel >> t) & 1u)) ok = issue_qk(t, j + kNS);
+          const int last = (sel >> 1) & 1u;  // the last tile that reads V(j)
+          bool v_landed = false;
           for (int t = 0; t < 2 && ok; ++t) {
-            if ((sel >> t) & 1u) {
-              ok = wait1(bar(BAR_PFULL + t), kept[t] & 1, wctx, H3_STATUS_TIMEOUT_MMA);
-              if (ok && !v_landed) ok = wait1(bar(BAR_VFULL + s), (j / kNS) & 1, wctx, H3_STATUS_TIMEOUT_MMA);
-              if (!ok) break;
-              v_landed = true;
-              tc_fence_after();
-              pv(t, s, kept[t] > 0);
-              ++kept[t];
-            }
+            if (!((sel >> t) & 1u)) continue;
+            ok = wait1(bar(BAR_PFULL + t), kept[t] & 1, wctx, H3_STATUS_TIMEOUT_MMA);
+            if (ok && !v_landed) ok = wait1(bar(BAR_VFULL + s), (j / kNS) & 1, wctx, H3_STATUS_TIMEOUT_MMA);
+            if (!ok) break;
+            v_landed = true;
+            tc_fence_after();
+            pv(t, s, kept[t] > 0);
+            ++kept[t];
+            sfree[t] = true;
             if (t == last) mma_commit(bar(BAR_VEMPTY + s));
-            if ((seln >> t) & 1u) {
-              if (!next_landed) {
-                ok = wait1(bar(BAR_KFULL + s2), use2 & 1, wctx, H3_STATUS_TIMEOUT_MMA);
-                if (!ok) break;
-                tc_fence_after();
-                next_landed = true;
-              }
-              qk(t, s2);
-              mma_commit(bar(BAR_SFULL + t));
-              if (t == last_k) mma_commit(bar(BAR_KEMPTY + s2));
-            }
+            ok = issue_qk(t, j + kNS);
           }
-          sel = seln;
         }
         if (ok)
           for (int t = 0; t < n_tiles; ++t)
