@@ -59,6 +59,21 @@ def test_host_pipeline_is_bitwise_the_device_path(wl, group):
     assert torch.equal(host["q"].view(torch.int16), g["q"].cpu().view(torch.int16))
 
 
+def test_host_pipeline_explicit_group_sizes():
+    w = W.workload("medium")
+    g = W.make_inputs(w, device="cuda")
+    host = {n: g[n].cpu().pin_memory() for n in ("q", "k", "v", "wq", "wk", "pos_thw")}
+    ref = h3.attention_block(g["q"].clone(), g["k"].clone(), g["v"], g["wq"], g["wk"], g["pos_thw"],
+                             g["cu_seqlens_q"], g["valid_len"], scale=SCALE)
+    pipe = h3.HostPipeline(w.q_rows, w.n_heads, group_sizes=[1, 20, 2, 19])
+    assert pipe.groups == [(0, 1), (1, 21), (21, 23), (23, 42)]
+    out = torch.full(ref.shape, float("nan"), dtype=torch.bfloat16).pin_memory()
+    pipe.run(host["q"], host["k"], host["v"], host["wq"], host["wk"], host["pos_thw"],
+             g["cu_seqlens_q"], g["valid_len"], out, scale=SCALE)
+    torch.cuda.current_stream().synchronize()
+    assert torch.equal(out.view(torch.int16), ref.cpu().view(torch.int16))
+
+
 def test_host_pipeline_attention_only_grouped():
     w = W.custom("grp", 5, [W.Segment(64, 64), W.Segment(200, 900), W.Segment(333, 1500)],
                  self_attention=False)
