@@ -75,9 +75,11 @@ enum {
 };
 constexpr uint32_t kOffTmemSlot = kOffBar + NUM_BARS * 8;
 constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
-constexpr uint32_t kOffList = kOffAbort + 4;  // block-sparse mode only
+// Block-sparse mode only: int [4] = union length, steps both tiles keep,
+// alternating pairs, the tile of the remaining steps; then the lists.
+constexpr uint32_t kOffList = kOffAbort + 4;
 constexpr uint32_t kListWords = kMaxSparseBlocks / 32;
-constexpr uint32_t kOffListBits = kOffList + 4;                    // [2][kListWords] u32
+constexpr uint32_t kOffListBits = kOffList + 16;                   // [2][kListWords] u32
 constexpr uint32_t kOffListTiles = kOffListBits + 2 * kListWords * 4;  // [kMaxSparseBlocks] u16
 constexpr uint32_t kOffListSel = kOffListTiles + kMaxSparseBlocks * 2;  // [kMaxSparseBlocks] u8
 constexpr uint32_t kSmemUsed = kOffList;
@@ -330,8 +332,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         r0 += __shfl_sync(0xffffffffu, i0, 31);
         r1 += __shfl_sync(0xffffffffu, i1, 31);
       }
-      const int base = nb + n0 + n1;
-      if (lane == 0) *reinterpret_cast<volatile int*>(gbase + kOffList) = base;
+      if (lane == 0) {
+        volatile int* hdr = reinterpret_cast<volatile int*>(gbase + kOffList);
+        hdr[0] = nb + n0 + n1;
+        hdr[1] = nb;
+        hdr[2] = m;
+        hdr[3] = n0 >= n1 ? 0 : 1;  // the tile of the steps after the alternation
+      }
     }
   }
 
@@ -563,79 +570,110 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
        }
       } else {
-        // Block-sparse: the steps walk the union of the two tiles' lists; a
-        // tile takes part only in the steps its own list keeps (no MMA for
-        // the others), and its S/P barrier phases count its kept steps.
-        // sel bit t: tile t keeps the step (bit 1 is never set for one tile).
-        //
-        // Each tile's next Q.K^T is issued as soon as (a) its previous P.V is
-        // issued (P aliases S) and (b) the K block is within the ring's reach:
-        // at step j the ring can hold K(j + 1) and K(j + 2), because every
-        // Q.K^T of step j was issued before step j.  Q_t.K(n)^T is thus issued
-        // by step n - 1 at the latest, and the tiles' chains interleave.
-        int kept[2] = {0, 0};
-        int nxt[2];         // tile t's next kept step whose Q.K^T is not issued (n_kv: none)
-        bool sfree[2] = {true, true};  // tile t's S/P columns may take a new Q.K^T
-        auto next_kept = [&](int t, int from) -> int {
-          int n = from;
-          while (n < n_kv && !((list_sel[n] >> t) & 1u)) ++n;
-          return n;
+        // Block-sparse.  The list builder orders the union of the two tiles'
+        // kept KV blocks in three phases: nb steps both tiles keep, then 2m
+        // steps alternating tile 0, tile 1 (tile 0 first), then the steps
+        // left to one tile (rt).  Each tile's next step is therefore known
+        // without a search, and every phase runs straight-line steps: the
+        // issuing thread pays tens of cycles for each branch or dependent
+        // scalar op between MMAs, while the MMA queue holds only a few.
+        // Every Q.K^T of step j is issued before step j, so K(j + 2) can
+        // always land; a K stage is released after its last Q.K^T, a V stage
+        // after its last P.V.  S/P barrier phases count each tile's steps.
+        const volatile int* hdr = reinterpret_cast<const volatile int*>(gbase + kOffList);
+        const int nb = hdr[1], m = hdr[2], rt = hdr[3];
+        const int na_end = nb + 2 * m;  // first step of the last phase
+        int kept0 = 0, kept1 = 0;
+        // tile t's first step after the two-tile phase (n_kv: none)
+        auto first_after_b = [&](int t) -> int {
+          if (m > 0) return nb + t;
+          return (na_end < n_kv && rt == t) ? na_end : n_kv;
         };
-        nxt[0] = next_kept(0, 0);
-        nxt[1] = next_kept(1, 0);
-        // Q_t.K(nxt[t])^T if allowed with the ring reaching step `reach`.
-        auto issue_qk = [&](int t, int reach) -> bool {
-          const int n = nxt[t];
-          if (!sfree[t] || n >= n_kv || n > reach) return true;
-          const int sn = n % kNS;
-          if (!wait1(bar(BAR_KFULL + sn), (n / kNS) & 1, wctx, H3_STATUS_TIMEOUT_MMA)) return false;
+        // Q_t.K(n)^T, t the last reader of K(n)
+        auto qk_last = [&](int t, int n) -> bool {
+          const uint32_t sn = static_cast<uint32_t>(n) & 1u;
+          if (!wait1(bar(BAR_KFULL + sn), (static_cast<uint32_t>(n) >> 1) & 1u, wctx,
+                     H3_STATUS_TIMEOUT_MMA))
+            return false;
           tc_fence_after();
-          qk(t, sn);
+          qk_(t ? dS1 : dS0, t ? qa1 : qa0, sn ? kb1 : kb0);
           mma_commit(bar(BAR_SFULL + t));
-          sfree[t] = false;
-          nxt[t] = next_kept(t, n + 1);
-          // The last reader of K(n) releases its stage.
-          const int o = t ^ 1;
-          if (!((list_sel[n] >> o) & 1u) || nxt[o] > n) mma_commit(bar(BAR_KEMPTY + sn));
+          mma_commit(bar(BAR_KEMPTY + sn));
           return true;
         };
-        if (ok) ok = issue_qk(0, kNS - 1) && issue_qk(1, kNS - 1);
-        for (int j = 0; j < n_kv && ok; ++j) {
-          const uint32_t sel = list_sel[j];
-          const uint32_t seln = j + 1 < n_kv ? static_cast<uint32_t>(list_sel[j + 1]) : 0u;
-          if ((sel & seln) == 3u) {
-            // Both tiles read V(j) and K(j + 1): the straight-line step.
-            ok = step2(j, static_cast<uint32_t>(kept[0]) & 1u, static_cast<uint32_t>(kept[1]) & 1u,
-                       kept[0] > 0 ? 1u : 0u, kept[1] > 0 ? 1u : 0u);
-            ++kept[0];
-            ++kept[1];
-            nxt[0] = next_kept(0, j + 2);
-            nxt[1] = next_kept(1, j + 2);
-            continue;
-          }
-          const int s = j % kNS;
-          // A tile idle at this step: its next Q.K^T may have come in reach.
-          for (int t = 0; t < 2 && ok; ++t)
-            if (!((sel >> t) & 1u)) ok = issue_qk(t, j + kNS);
-          const int last = (sel >> 1) & 1u;  // the last tile that reads V(j)
-          bool v_landed = false;
-          for (int t = 0; t < 2 && ok; ++t) {
-            if (!((sel >> t) & 1u)) continue;
-            ok = wait1(bar(BAR_PFULL + t), kept[t] & 1, wctx, H3_STATUS_TIMEOUT_MMA);
-            if (ok && !v_landed) ok = wait1(bar(BAR_VFULL + s), (j / kNS) & 1, wctx, H3_STATUS_TIMEOUT_MMA);
-            if (!ok) break;
-            v_landed = true;
+        // P_t.V(j), t the last reader of V(j)
+        auto pv_last = [&](int t, int j, int kept) -> bool {
+          const uint32_t s = static_cast<uint32_t>(j) & 1u;
+          bool r = wait1(bar(BAR_PFULL + t), static_cast<uint32_t>(kept) & 1u, wctx,
+                         H3_STATUS_TIMEOUT_MMA);
+          r &= wait1(bar(BAR_VFULL + s), (static_cast<uint32_t>(j) >> 1) & 1u, wctx,
+                     H3_STATUS_TIMEOUT_MMA);
+          tc_fence_after();
+          pv_(t ? dO1 : dO0, t ? dS1 : dS0, s ? vb1 : vb0, kept > 0 ? 1u : 0u);
+          mma_commit(bar(BAR_VEMPTY + s));
+          return r;
+        };
+        if (ok) {
+          if (nb > 0) {
             tc_fence_after();
-            pv(t, s, kept[t] > 0);
-            ++kept[t];
-            sfree[t] = true;
-            if (t == last) mma_commit(bar(BAR_VEMPTY + s));
-            ok = issue_qk(t, j + kNS);
+            qk_(dS0, qa0, kb0);
+            mma_commit(bar(BAR_SFULL));
+            qk_(dS1, qa1, kb0);
+            mma_commit(bar(BAR_SFULL + 1));
+            mma_commit(bar(BAR_KEMPTY));
+          } else {
+            const int f0 = first_after_b(0), f1 = first_after_b(1);
+            if (f0 < n_kv) ok = qk_last(0, f0);
+            if (ok && f1 < n_kv) ok = qk_last(1, f1);
           }
         }
-        if (ok)
-          for (int t = 0; t < n_tiles; ++t)
-            if (kept[t] > 0) mma_commit(bar(BAR_OFINAL + t));
+        // Two-tile phase: the dense kernel's step, then the last step hands
+        // each tile over to its first step after the phase.
+        int j = 0;
+        for (; j + 1 < nb && ok; ++j) {
+          ok = step2(j, static_cast<uint32_t>(kept0) & 1u, static_cast<uint32_t>(kept1) & 1u,
+                     kept0 > 0 ? 1u : 0u, kept1 > 0 ? 1u : 0u);
+          ++kept0;
+          ++kept1;
+        }
+        if (ok && nb > 0) {
+          const uint32_t s = static_cast<uint32_t>(j) & 1u;
+          ok = wait1(bar(BAR_PFULL), static_cast<uint32_t>(kept0) & 1u, wctx, H3_STATUS_TIMEOUT_MMA);
+          ok &= wait1(bar(BAR_VFULL + s), (static_cast<uint32_t>(j) >> 1) & 1u, wctx,
+                      H3_STATUS_TIMEOUT_MMA);
+          tc_fence_after();
+          pv_(dO0, dS0, s ? vb1 : vb0, kept0 > 0 ? 1u : 0u);
+          ++kept0;
+          const int f0 = first_after_b(0), f1 = first_after_b(1);
+          if (ok && f0 < n_kv) ok = qk_last(0, f0);
+          ok &= wait1(bar(BAR_PFULL + 1), static_cast<uint32_t>(kept1) & 1u, wctx,
+                      H3_STATUS_TIMEOUT_MMA);
+          tc_fence_after();
+          pv_(dO1, dS1, s ? vb1 : vb0, kept1 > 0 ? 1u : 0u);
+          mma_commit(bar(BAR_VEMPTY + s));
+          ++kept1;
+          if (ok && f1 < n_kv) ok = qk_last(1, f1);
+          ++j;
+        }
+        // Alternating phase: step j belongs to tile (j - nb) & 1, whose next
+        // step is j + 2, or the first step of the last phase.
+        for (; j < na_end && ok; ++j) {
+          const int a = (j - nb) & 1;
+          ok = pv_last(a, j, a ? kept1 : kept0);
+          if (a) ++kept1; else ++kept0;
+          const int na = j + 2 < na_end ? j + 2 : ((rt == a && na_end < n_kv) ? na_end : n_kv);
+          if (ok && na < n_kv) ok = qk_last(a, na);
+        }
+        // Last phase: one tile, step after step.
+        for (; j < n_kv && ok; ++j) {
+          ok = pv_last(rt, j, rt ? kept1 : kept0);
+          if (rt) ++kept1; else ++kept0;
+          if (ok && j + 1 < n_kv) ok = qk_last(rt, j + 1);
+        }
+        if (ok) {
+          if (kept0 > 0) mma_commit(bar(BAR_OFINAL));
+          if (kept1 > 0) mma_commit(bar(BAR_OFINAL + 1));
+        }
       }
       // Every MMA issued above completes before TMEM is released.
       mma_commit(bar(BAR_DRAIN));
