@@ -166,6 +166,17 @@ __device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, const WaitC
   }
 }
 
+// Two bounded waits whose first try_waits are issued back to back: two
+// barriers that have already completed cost one round trip, not two.
+__device__ __forceinline__ bool wait2(uint32_t bar_a, uint32_t par_a, uint32_t bar_b, uint32_t par_b,
+                                      const WaitCtx& w, uint32_t bit) {
+  const bool a = mbar_try_wait(bar_a, par_a);
+  const bool b = mbar_try_wait(bar_b, par_b);
+  if (a && b) return true;
+  if (!a && !wait1(bar_a, par_a, w, bit)) return false;
+  return b || wait1(bar_b, par_b, w, bit);
+}
+
 // Bounded wait that only ends on completion or time (no early stop): used to
 // drain operations already in flight before the CTA exits.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -482,9 +493,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       auto step2 = [&](int j, uint32_t pp0, uint32_t pp1, uint32_t acc0, uint32_t acc1) -> bool {
         const uint32_t s = static_cast<uint32_t>(j) & 1u;
         const uint64_t vbc = s ? vb1 : vb0, kbn = s ? kb0 : kb1;  // V of this stage, K of the next
-        bool r = wait1(bar(BAR_PFULL), pp0, wctx, H3_STATUS_TIMEOUT_MMA);
-        r &= wait1(bar(BAR_VFULL + s), (static_cast<uint32_t>(j) >> 1) & 1u, wctx,
-                   H3_STATUS_TIMEOUT_MMA);
+        bool r = wait2(bar(BAR_PFULL), pp0, bar(BAR_VFULL + s), (static_cast<uint32_t>(j) >> 1) & 1u,
+                       wctx, H3_STATUS_TIMEOUT_MMA);
         tc_fence_after();
         pv_(dO0, dS0, vbc, acc0);
         r &= wait1(bar(BAR_KFULL + (s ^ 1u)), (static_cast<uint32_t>(j + 1) >> 1) & 1u, wctx,
@@ -521,9 +531,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           const uint32_t s = static_cast<uint32_t>(j) & 1u;
           const uint64_t vbc = s ? vb1 : vb0;
           const uint32_t acc = j > 0 ? 1u : 0u;
-          ok = wait1(bar(BAR_PFULL), s, wctx, H3_STATUS_TIMEOUT_MMA);
-          ok &= wait1(bar(BAR_VFULL + s), (static_cast<uint32_t>(j) >> 1) & 1u, wctx,
-                      H3_STATUS_TIMEOUT_MMA);
+          ok = wait2(bar(BAR_PFULL), s, bar(BAR_VFULL + s), (static_cast<uint32_t>(j) >> 1) & 1u,
+                     wctx, H3_STATUS_TIMEOUT_MMA);
           tc_fence_after();
           pv_(dO0, dS0, vbc, acc);
           mma_commit(bar(BAR_OFINAL));
@@ -604,10 +613,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         // P_t.V(j), t the last reader of V(j)
         auto pv_last = [&](int t, int j, int kept) -> bool {
           const uint32_t s = static_cast<uint32_t>(j) & 1u;
-          bool r = wait1(bar(BAR_PFULL + t), static_cast<uint32_t>(kept) & 1u, wctx,
-                         H3_STATUS_TIMEOUT_MMA);
-          r &= wait1(bar(BAR_VFULL + s), (static_cast<uint32_t>(j) >> 1) & 1u, wctx,
-                     H3_STATUS_TIMEOUT_MMA);
+          const bool r = wait2(bar(BAR_PFULL + t), static_cast<uint32_t>(kept) & 1u, bar(BAR_VFULL + s),
+                               (static_cast<uint32_t>(j) >> 1) & 1u, wctx, H3_STATUS_TIMEOUT_MMA);
           tc_fence_after();
           pv_(t ? dO1 : dO0, t ? dS1 : dS0, s ? vb1 : vb0, kept > 0 ? 1u : 0u);
           mma_commit(bar(BAR_VEMPTY + s));
@@ -638,9 +645,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
         if (ok && nb > 0) {
           const uint32_t s = static_cast<uint32_t>(j) & 1u;
-          ok = wait1(bar(BAR_PFULL), static_cast<uint32_t>(kept0) & 1u, wctx, H3_STATUS_TIMEOUT_MMA);
-          ok &= wait1(bar(BAR_VFULL + s), (static_cast<uint32_t>(j) >> 1) & 1u, wctx,
-                      H3_STATUS_TIMEOUT_MMA);
+          ok = wait2(bar(BAR_PFULL), static_cast<uint32_t>(kept0) & 1u, bar(BAR_VFULL + s),
+                     (static_cast<uint32_t>(j) >> 1) & 1u, wctx, H3_STATUS_TIMEOUT_MMA);
           tc_fence_after();
           pv_(dO0, dS0, s ? vb1 : vb0, kept0 > 0 ? 1u : 0u);
           ++kept0;
