@@ -493,13 +493,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       auto step2 = [&](int j, uint32_t pp0, uint32_t pp1, uint32_t acc0, uint32_t acc1) -> bool {
         const uint32_t s = static_cast<uint32_t>(j) & 1u;
         const uint64_t vbc = s ? vb1 : vb0, kbn = s ? kb0 : kb1;  // V of this stage, K of the next
-        bool r = wait2(bar(BAR_PFULL), pp0, bar(BAR_VFULL + s), (static_cast<uint32_t>(j) >> 1) & 1u,
-                       wctx, H3_STATUS_TIMEOUT_MMA);
+        // The step's P and V try_waits and a test of K go out back to back;
+        // K, needed only after the first P.V, is waited for there if it had
+        // not landed.
+        const uint32_t kbar = bar(BAR_KFULL + (s ^ 1u)), kpar = (static_cast<uint32_t>(j + 1) >> 1) & 1u;
+        const bool p_ok = mbar_try_wait(bar(BAR_PFULL), pp0);
+        const bool v_ok = mbar_try_wait(bar(BAR_VFULL + s), (static_cast<uint32_t>(j) >> 1) & 1u);
+        const bool k_ok = mbar_test_wait(kbar, kpar);  // a probe: K must not hold up P.V
+        bool r = p_ok || wait1(bar(BAR_PFULL), pp0, wctx, H3_STATUS_TIMEOUT_MMA);
+        r = r && (v_ok || wait1(bar(BAR_VFULL + s), (static_cast<uint32_t>(j) >> 1) & 1u, wctx,
+                                H3_STATUS_TIMEOUT_MMA));
         tc_fence_after();
         pv_(dO0, dS0, vbc, acc0);
-        r &= wait1(bar(BAR_KFULL + (s ^ 1u)), (static_cast<uint32_t>(j + 1) >> 1) & 1u, wctx,
-                   H3_STATUS_TIMEOUT_MMA);
-        tc_fence_after();
+        if (!k_ok) {
+          r = r && wait1(kbar, kpar, wctx, H3_STATUS_TIMEOUT_MMA);
+          tc_fence_after();
+        }
         qk_(dS0, qa0, kbn);
         mma_commit(bar(BAR_SFULL));
         r &= wait1(bar(BAR_PFULL + 1), pp1, wctx, H3_STATUS_TIMEOUT_MMA);
@@ -610,15 +619,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           mma_commit(bar(BAR_KEMPTY + sn));
           return true;
         };
-        // P_t.V(j), t the last reader of V(j)
-        auto pv_last = [&](int t, int j, int kept) -> bool {
-          const uint32_t s = static_cast<uint32_t>(j) & 1u;
-          const bool r = wait2(bar(BAR_PFULL + t), static_cast<uint32_t>(kept) & 1u, bar(BAR_VFULL + s),
-                               (static_cast<uint32_t>(j) >> 1) & 1u, wctx, H3_STATUS_TIMEOUT_MMA);
+        // P_t.V(j) then Q_t.K(n)^T (n < n_kv), t the last reader of V(j) and
+        // of K(n); the P and V try_waits and a test of K go out back to back.
+        auto step1 = [&](int t, int j, int kept, int n) -> bool {
+          const uint32_t s = static_cast<uint32_t>(j) & 1u, sn = static_cast<uint32_t>(n) & 1u;
+          const uint32_t pbar = bar(BAR_PFULL + t), ppar = static_cast<uint32_t>(kept) & 1u;
+          const uint32_t vbar = bar(BAR_VFULL + s), vpar = (static_cast<uint32_t>(j) >> 1) & 1u;
+          const uint32_t kbar = bar(BAR_KFULL + sn), kpar = (static_cast<uint32_t>(n) >> 1) & 1u;
+          const bool p_ok = mbar_try_wait(pbar, ppar);
+          const bool v_ok = mbar_try_wait(vbar, vpar);
+          const bool k_ok = n >= n_kv || mbar_test_wait(kbar, kpar);  // a probe: K must not hold up P.V
+          bool r = p_ok || wait1(pbar, ppar, wctx, H3_STATUS_TIMEOUT_MMA);
+          r = r && (v_ok || wait1(vbar, vpar, wctx, H3_STATUS_TIMEOUT_MMA));
+          if (!r) return false;
           tc_fence_after();
           pv_(t ? dO1 : dO0, t ? dS1 : dS0, s ? vb1 : vb0, kept > 0 ? 1u : 0u);
           mma_commit(bar(BAR_VEMPTY + s));
-          return r;
+          if (n >= n_kv) return true;
+          if (!k_ok) {
+            if (!wait1(kbar, kpar, wctx, H3_STATUS_TIMEOUT_MMA)) return false;
+            tc_fence_after();
+          }
+          qk_(t ? dS1 : dS0, t ? qa1 : qa0, sn ? kb1 : kb0);
+          mma_commit(bar(BAR_SFULL + t));
+          mma_commit(bar(BAR_KEMPTY + sn));
+          return true;
         };
         if (ok) {
           if (nb > 0) {
@@ -665,16 +690,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         // step is j + 2, or the first step of the last phase.
         for (; j < na_end && ok; ++j) {
           const int a = (j - nb) & 1;
-          ok = pv_last(a, j, a ? kept1 : kept0);
-          if (a) ++kept1; else ++kept0;
           const int na = j + 2 < na_end ? j + 2 : ((rt == a && na_end < n_kv) ? na_end : n_kv);
-          if (ok && na < n_kv) ok = qk_last(a, na);
+          ok = step1(a, j, a ? kept1 : kept0, na);
+          if (a) ++kept1; else ++kept0;
         }
         // Last phase: one tile, step after step.
         for (; j < n_kv && ok; ++j) {
-          ok = pv_last(rt, j, rt ? kept1 : kept0);
+          ok = step1(rt, j, rt ? kept1 : kept0, j + 1);
           if (rt) ++kept1; else ++kept0;
-          if (ok && j + 1 < n_kv) ok = qk_last(rt, j + 1);
         }
         if (ok) {
           if (kept0 > 0) mma_commit(bar(BAR_OFINAL));
