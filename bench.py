@@ -370,15 +370,7 @@ def bench_gpu(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 Q/K/V, N(1,0.1) norm weights, garbage pads)",
-        "config": {"workload": w.name, "description": w.description,
-                   "valid_tokens": [s.n_valid_q() for s in w.segments],
-                   "buffer_rows": [s.q_rows for s in w.segments],
-                   "heads": w.n_heads, "head_dim": 128,
-                   "attention_flop_per_step": flops,
-                   "prologue_bytes_per_step": w.prologue_bytes(),
-                   "l2": "inputs larger than L2 (Q,K,V 632 MB each); no flush"
-                   if w.name == "full" else "no flush",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": workload_config(w, world),
         "roofline": {"bound": "tensor", "achieved": round(attn_tflops, 2),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(attn_tflops / peak, 4),
                      "frac_of_burst": round(attn_tflops / pk["bf16"], 4),
@@ -595,6 +587,19 @@ def committed_traffic(w):
 
 
 # -------------------------------------------------------- the reference arm
+def workload_config(w, world):
+    """The `config` object of the JSON line; both arms report the same one."""
+    return {"workload": w.name, "description": w.description,
+            "valid_tokens": [s.n_valid_q() for s in w.segments],
+            "buffer_rows": [s.q_rows for s in w.segments],
+            "heads": w.n_heads, "head_dim": 128,
+            "attention_flop_per_step": w.attention_flops(),
+            "prologue_bytes_per_step": w.prologue_bytes(),
+            "l2": "inputs larger than L2 (Q,K,V 632 MB each); no flush"
+            if w.name == "full" else "no flush",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
 def bench_reference(args):
     """The CPU oracle timed as the reference arm: each step is a bounded
     sample (args.ref_rows query rows x args.ref_heads heads) of the workload."""
@@ -618,7 +623,7 @@ def bench_reference(args):
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "heads": w.n_heads, "head_dim": 128},
+        "config": workload_config(w, int(os.environ.get("WORLD_SIZE", "1"))),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(),
                          "kind": "oracle", "sample": vals[-1]["sample"]},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
