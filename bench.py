@@ -556,15 +556,25 @@ def wire_timing(h3, g, w, stream, pk, iters=5):
     return res
 
 
+def _code_only(text):
+    """Source text without comments, trailing spaces or blank lines, so that a
+    comment edit does not count as a kernel change."""
+    import re
+    text = re.sub(rb"/\*.*?\*/", b"", text, flags=re.S)
+    text = re.sub(rb"//[^\n]*", b"", text)
+    return b"\n".join(l.rstrip() for l in text.split(b"\n") if l.strip())
+
+
 def kernel_source_digest():
-    """First 16 hex digits of sha256 over the attention kernel's device code:
-    attention.cu up to its host-side section, then ptx.cuh."""
+    """First 16 hex digits of sha256 over the attention kernel's device code,
+    comments left out: attention.cu up to its host-side section, then ptx.cuh."""
     import hashlib
     csrc = os.path.join(ROOT, "packed_sequence_attention_gb300", "csrc")
     text = open(os.path.join(csrc, "attention.cu"), "rb").read()
     cut = text.find(b"// ------------------------------------------------------------------ host side")
     device = text if cut < 0 else text[:cut]
-    return hashlib.sha256(device + open(os.path.join(csrc, "ptx.cuh"), "rb").read()).hexdigest()[:16]
+    ptx = open(os.path.join(csrc, "ptx.cuh"), "rb").read()
+    return hashlib.sha256(_code_only(device) + b"\n" + _code_only(ptx)).hexdigest()[:16]
 
 
 def committed_traffic(w):

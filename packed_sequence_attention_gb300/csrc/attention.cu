@@ -230,9 +230,10 @@ __device__ __forceinline__ void zero_fill(const AttnParams& p) {
 }
 
 // kSparse: Sol-Attn block-sparse mode -- one packed sequence, each query
-// tile attends to the KV tiles its block list keeps; a CTA walks the ordered
-// union of its two tiles' lists and a tile not kept by one query tile
-// contributes P = 0 there.
+// tile attends to the KV tiles its block list keeps.  A CTA walks the union
+// of its two tiles' lists (both-kept blocks, then the tiles' own blocks
+// alternating, then the longer list's rest); a tile takes part only in the
+// steps its list keeps.
 template <bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
