@@ -359,9 +359,10 @@ def head_groups(n_heads: int, heads_per_group: int = 6,
     ``group_sizes`` gives them explicitly (positive, summing to ``n_heads``).
     Otherwise groups hold up to ``heads_per_group`` heads, except that with
     more than two groups the first and the last hold half of that (at least
-    one head) and the ones between share the rest evenly.  Only the first group's copy in and the last group's copy out are
-    not hidden behind compute, so smaller end groups shorten the step; much
-    smaller ones make narrow 2-D copies, which move fewer bytes per second.
+    one head) and the ones between share the rest evenly.  Only the first
+    group's copy in and the last group's copy out are not hidden behind
+    compute, so smaller end groups shorten the step; much smaller ones make
+    narrow 2-D copies, which move fewer bytes per second.
     (42 heads, 6 per group, on GB300: 49.2 ms per step with seven groups of
     6, 48.6 ms with [3, 6 x 6, 3], 48.9 ms with [2, 4, 6 x 5, 4, 2].)"""
     if group_sizes is not None:
