@@ -168,6 +168,13 @@ def _mask(kind, H, nb):
                 keep[:, a, b] = (a % 2 == 1) and (b >= a // 2)
             elif kind == "single_shared":   # both tiles keep only the last block
                 keep[:, a, b] = b == nb - 1
+            elif kind in ("phases_r1", "phases_r0"):
+                # all three step phases: blocks 0-1 kept by both tiles, then
+                # each tile's own blocks, one tile with two more than the other
+                mine = ({0, 1, 2, 4}, {0, 1, 3, 5, 6, 7})
+                if kind == "phases_r0":
+                    mine = mine[::-1]
+                keep[:, a, b] = b in mine[a % 2]
     if kind == "per_head":
         rng = np.random.default_rng(11)
         keep = rng.random((H, nb, nb)) < 0.3
@@ -176,7 +183,7 @@ def _mask(kind, H, nb):
 
 
 @pytest.mark.parametrize("kind", ["even_odd", "one_tile_empty", "first_tile_empty",
-                                  "single_shared", "per_head"])
+                                  "single_shared", "phases_r1", "phases_r0", "per_head"])
 def test_sparse_attention_tiles_with_different_lists(kind):
     H, rows = 3, 1000                        # 8 blocks, the last one partial (104 rows)
     nb = -(-rows // B)
