@@ -229,13 +229,18 @@ def bench_gpu(args):
     # ---- device-resident inputs (seeded, generated on the GPU)
     g = W.make_inputs(w, device=f"cuda:{local}", seed=W.default_seed(w) + rank)
     stream = torch.cuda.current_stream()
-    if args.wire_only:
+    if args.wire_only or args.next_only:
         if not w.self_attention:
-            raise SystemExit("--wire-only needs a self-attention workload")
-        res = wire_timing(h3, g, w, stream, pk)
+            raise SystemExit("--wire-only / --next-only need a self-attention workload")
+        if args.wire_only:
+            res = {"wire_formats": wire_timing(h3, g, w, stream, pk)}
+        else:
+            res = {"lora_prologue": lora_prologue_timing(h3, g, w, stream, pk),
+                   "sol_block_sparse": sol_attention_timing(h3, g, w, stream, pk)}
+        if h3.status_word():
+            raise SystemExit("device status word is nonzero after the timed calls")
         if rank == 0:
-            print(json.dumps({"workload": w.name, "rows": w.segments[0].n_valid_q(),
-                              "wire_formats": res}))
+            print(json.dumps({"workload": w.name, "rows": w.segments[0].n_valid_q(), **res}))
         if dist is not None:
             dist.destroy_process_group()
         return
@@ -511,7 +516,7 @@ def sol_attention_timing(h3, g, w, stream, pk, tau=1.0, iters=5):
     t /= iters
     nb = -(-n // 128)
     kept = float(counts.double().sum().item()) / (w.n_heads * nb * nb)
-    flops_kept = kept * w.attention_flops()
+    flops_kept = kept * 4.0 * w.n_heads * 128 * n * n  # the first sequence only
     total_ms = float(t.sum())
     return {"tau": tau, "kept_fraction": round(kept, 4), "means_ms": round(t[0], 3),
             "select_ms": round(t[1], 3), "attention_ms": round(t[2], 3),
@@ -658,6 +663,8 @@ def main():
                     help="profiling mode: warm-up and timed steps only (no e2e, no CPU baseline)")
     ap.add_argument("--wire-only", action="store_true",
                     help="profiling mode: the wire-format kernels on the first sequence only")
+    ap.add_argument("--next-only", action="store_true",
+                    help="profiling mode: the LoRA-fused prologue and the Sol-Attn stages only")
     args = ap.parse_args()
     if args.impl == "reference":
         bench_reference(args)
