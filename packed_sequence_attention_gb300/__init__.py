@@ -328,13 +328,18 @@ def attention_block(q, k, v, wq, wk, pos_thw, cu_seqlens, valid_len,
     """The block's hot path: fused Q/K norm + RoPE on the valid rows of each
     packed sequence, then attention over the valid rows.  Q and K are
     modified in place."""
+    _block_prologue(q, k, wq, wk, pos_thw, cu_seqlens, valid_len, rot, theta, eps, stream)
+    return attention(q, k, v, cu_seqlens, cu_seqlens, valid_len, scale, out, stream)
+
+
+def _block_prologue(q, k, wq, wk, pos_thw, cu_seqlens, valid_len, rot, theta, eps, stream):
+    """The norm + RoPE of ``attention_block``: each packed sequence's valid rows."""
     for b in range(len(cu_seqlens) - 1):
         r0 = cu_seqlens[b]
         n = valid_len[b] if valid_len is not None else cu_seqlens[b + 1] - r0
         if n:
             qk_norm_rope(q[r0:], k[r0:], wq, wk, pos_thw[r0:], n_rows=n, rot=rot,
                          theta=theta, eps=eps, stream=stream)
-    return attention(q, k, v, cu_seqlens, cu_seqlens, valid_len, scale, out, stream)
 
 
 def copy_2d(dst: torch.Tensor, src: torch.Tensor, stream=None) -> None:
@@ -440,19 +445,23 @@ class HostPipeline:
         synchronise on it (or an event recorded on it) sees ``out`` filled.
         Q, K, V, weights and positions are read from the host tensors; the
         device copies of Q and K are normalised in place."""
+        # The prologue of a group needs only its Q and K: it runs while the
+        # group's V is still being copied in.
+        def prologue(h0, h1, sc):
+            _block_prologue(self.q[:, h0:h1], self.k[:, h0:h1], self.wq[h0:h1], self.wk[h0:h1],
+                            self.pos, cu_seqlens, valid_len, rot, theta, eps, sc)
+
         def compute(h0, h1, sc):
-            attention_block(self.q[:, h0:h1], self.k[:, h0:h1], self.v[:, h0:h1],
-                            self.wq[h0:h1], self.wk[h0:h1], self.pos, cu_seqlens, valid_len,
-                            rot=rot, theta=theta, eps=eps, scale=scale,
-                            out=self.out[:, h0:h1], stream=sc)
+            attention(self.q[:, h0:h1], self.k[:, h0:h1], self.v[:, h0:h1], cu_seqlens,
+                      cu_seqlens, valid_len, scale, self.out[:, h0:h1], sc)
 
         def small_inputs():
             self.wq.copy_(wq, non_blocking=True)
             self.wk.copy_(wk, non_blocking=True)
             self.pos.copy_(pos_thw, non_blocking=True)
-        self._pipeline(q, k, v, out, compute, small_inputs, stream)
+        self._pipeline(q, k, v, out, compute, small_inputs, stream, prologue)
 
-    def _pipeline(self, q, k, v, out, compute, small_inputs, stream):
+    def _pipeline(self, q, k, v, out, compute, small_inputs, stream, prologue=None):
         cur = stream if stream is not None else torch.cuda.current_stream()
         start = torch.cuda.Event()
         start.record(cur)
@@ -462,11 +471,17 @@ class HostPipeline:
             with torch.cuda.stream(self.s_in):
                 small_inputs()
         for i, (h0, h1) in enumerate(self.groups):
-            for dev_t, host_t in ((self.q, q), (self.k, k), (self.v, v)):
+            sc = self.s_comp[i % 2]
+            for dev_t, host_t in ((self.q, q), (self.k, k)):
                 copy_2d(dev_t[:, h0:h1], host_t[:, h0:h1], self.s_in)
+            if prologue is not None:
+                qk_landed = torch.cuda.Event()
+                qk_landed.record(self.s_in)
+                sc.wait_event(qk_landed)
+                prologue(h0, h1, sc)
+            copy_2d(self.v[:, h0:h1], v[:, h0:h1], self.s_in)
             landed = torch.cuda.Event()
             landed.record(self.s_in)
-            sc = self.s_comp[i % 2]
             sc.wait_event(landed)
             compute(h0, h1, sc)
             done = torch.cuda.Event()
