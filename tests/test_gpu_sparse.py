@@ -201,3 +201,26 @@ def test_sparse_attention_tiles_with_different_lists(kind):
             if none[h, a]:
                 assert (got[a * B:(a + 1) * B, h] == 0).all(), f"head {h} block {a} not zero"
     gate(got, ref, kind)
+
+
+def test_sparse_attention_at_the_block_limit():
+    """2,048 KV blocks (the most a sequence may have; the last one ragged):
+    the union bitmaps span all 64 words.  Sampled rows against the oracle."""
+    H, rows = 1, 2048 * B - 37
+    nb = -(-rows // B)
+    q, k, v = inputs(H, rows, seed=31)
+    keep = np.zeros((H, nb, nb), dtype=bool)
+    for a in range(nb):
+        for b in (0, 1, a, (a * 7919 + 13) % nb, nb - 1):
+            keep[:, a, b] = True
+    lists, counts = _lists_from_mask(keep)
+    out = torch.full((rows, H, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    h3.sparse_attention(q, k, v, lists, counts, rows, SCALE, out=out)
+    torch.cuda.synchronize()
+    sample = np.array(sorted({0, 1, 127, 128, 255, 256, 4095, 65536, 131071, 131072,
+                              rows - 129, rows - 128, rows - 91, rows - 1} |
+                             set(np.random.default_rng(5).integers(0, rows, 12).tolist())))
+    ref = O.block_sparse_attention(O.widen(q), O.widen(k), O.widen(v), rows, keep, B, SCALE,
+                                   rows=sample)
+    got = O.widen(out)[sample]
+    gate(got, ref, "block limit")
