@@ -427,6 +427,9 @@ class HostPipeline:
         self.s_in = torch.cuda.Stream(device=dev)
         self.s_out = torch.cuda.Stream(device=dev)
         self.s_comp = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
+        # Prologues run on a stream of their own, each as soon as its group's
+        # Q and K have landed, so that attention launches follow one another.
+        self.s_pro = torch.cuda.Stream(device=dev, priority=-1)
 
     def run_attention(self, q, k, v, cu_seqlens_q, cu_seqlens_kv, valid_len, out, scale=None,
                       stream=None) -> None:
@@ -445,8 +448,8 @@ class HostPipeline:
         synchronise on it (or an event recorded on it) sees ``out`` filled.
         Q, K, V, weights and positions are read from the host tensors; the
         device copies of Q and K are normalised in place."""
-        # The prologue of a group needs only its Q and K: it runs while the
-        # group's V is still being copied in.
+        # The prologue of a group needs only its Q and K: it runs (on its own
+        # stream) while the group's V is still being copied in.
         def prologue(h0, h1, sc):
             _block_prologue(self.q[:, h0:h1], self.k[:, h0:h1], self.wq[h0:h1], self.wk[h0:h1],
                             self.pos, cu_seqlens, valid_len, rot, theta, eps, sc)
@@ -465,7 +468,7 @@ class HostPipeline:
         cur = stream if stream is not None else torch.cuda.current_stream()
         start = torch.cuda.Event()
         start.record(cur)
-        for s in (self.s_in, self.s_out, *self.s_comp):
+        for s in (self.s_in, self.s_out, *self.s_comp, self.s_pro):
             s.wait_event(start)
         if small_inputs is not None:
             with torch.cuda.stream(self.s_in):
@@ -477,8 +480,11 @@ class HostPipeline:
             if prologue is not None:
                 qk_landed = torch.cuda.Event()
                 qk_landed.record(self.s_in)
-                sc.wait_event(qk_landed)
-                prologue(h0, h1, sc)
+                self.s_pro.wait_event(qk_landed)
+                prologue(h0, h1, self.s_pro)
+                normed = torch.cuda.Event()
+                normed.record(self.s_pro)
+                sc.wait_event(normed)
             copy_2d(self.v[:, h0:h1], v[:, h0:h1], self.s_in)
             landed = torch.cuda.Event()
             landed.record(self.s_in)
@@ -488,7 +494,7 @@ class HostPipeline:
             done.record(sc)
             self.s_out.wait_event(done)
             copy_2d(out[:, h0:h1], self.out[:, h0:h1], self.s_out)
-        for s in (self.s_out, *self.s_comp):
+        for s in (self.s_out, *self.s_comp, self.s_pro):
             ev = torch.cuda.Event()
             ev.record(s)
             cur.wait_event(ev)
