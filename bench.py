@@ -50,7 +50,8 @@ def peaks():
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "clocks.mem")
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
@@ -78,7 +79,7 @@ class ClockSampler:
             self.lines = [l for l in out.splitlines() if l.strip()]
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
+        sm, mx, mem, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in getattr(self, "lines", []):
             f = [x.strip() for x in line.split(",")]
@@ -92,9 +93,14 @@ class ClockSampler:
             for name, val in zip(names, f[5:9]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
+            try:
+                mem.append(float(f[9]))
+            except (IndexError, ValueError):
+                pass
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx),
+                "mem_mhz": float(np.median(mem)) if mem else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
