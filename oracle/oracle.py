@@ -390,20 +390,3 @@ def out_fp8_records(o) -> np.ndarray:
     """[rows, H, D] -> uint8 [rows, H, 128] raw E4M3 bytes, no scale."""
     return e4m3_bits(e4m3_round(o))
 
-
-def attention_flops(cu_seqlens_q, cu_seqlens_kv, valid_len, n_heads: int,
-                    head_dim: int, rows=None) -> float:
-    """Valid-token multiply-add count * 2 of the two products (4*H*D*Lq*Lkv),
-    restricted to ``rows`` when given."""
-    total = 0.0
-    for b in range(len(cu_seqlens_q) - 1):
-        q0, q1 = cu_seqlens_q[b], cu_seqlens_q[b + 1]
-        nq = q1 - q0
-        nkv = cu_seqlens_kv[b + 1] - cu_seqlens_kv[b]
-        if valid_len is not None:
-            nq = nkv = valid_len[b]
-        if rows is not None:
-            r = np.asarray(rows)
-            nq = int(np.count_nonzero((r >= q0) & (r < q0 + nq)))
-        total += 4.0 * n_heads * head_dim * nq * nkv
-    return total

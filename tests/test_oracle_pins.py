@@ -390,6 +390,100 @@ def pin_wire_records(Ox):
     return worst
 
 
+def pin_int8_ties_and_clamp(Ox):
+    """Block-INT8 quantiser by hand (Sol-H3 section 3.2 "Quantized
+    communication"; the tie and clamp rules are the reading taken there).
+
+    A group whose largest magnitude is 126.5 * 1.125 takes code 0x79
+    (127 * 1.0 < 142.3125 <= 127 * 1.125), so every value below is an exact
+    multiple of s = 1.125; exact half-integer quotients round to the even
+    integer: +-0.5 -> 0, +-1.5 -> +-2, +-2.5 -> +-2, +-3.5 -> +-4,
+    +-126.5 -> +-126.  A second group at code 0x80 (s = 2) repeats a tie at a
+    different scale.  A group past the largest code (255, value 122880) is
+    clamped to the symmetric range: +-127, never -128."""
+    s = 1.125
+    quot = [0.5, -0.5, 1.5, -1.5, 2.5, -2.5, 3.5, -3.5, 126.5, -126.5, 0.25, 100.75, -7.0]
+    want = [0, 0, 2, -2, 2, -2, 4, -4, 126, -126, 0, 101, -7]
+    x = np.zeros((1, 128))
+    x[0, :len(quot)] = np.array(quot) * s
+    # group 1: s = 2 (amax 125.5 * 2 = 251 lies in (127 * 1.875, 127 * 2])
+    x[0, 32:36] = np.array([125.5, 0.5, -4.5, 9.0]) * 2.0
+    want1 = [126, 0, -4, 9]
+    # group 2: code 255, value 2^16 * 1.875 = 122880; 127 * value = 15,605,760
+    x[0, 64:70] = [2.0e7, -2.0e7, -1.6e7, 15605760.0, -15605760.0, 122880.0 * 126.5]
+    want2 = [127, -127, -127, 127, -127, 126]
+    vals, codes = Ox.int8_group32(x)
+    v = vals.astype(np.int64)[0]
+    ok = (list(codes[0]) == [0x79, 0x80, 0xFF, 0x00] and list(v[:len(want)]) == want and
+          list(v[32:36]) == want1 and list(v[64:70]) == want2 and
+          not v[len(want):32].any() and not v[96:].any())
+    return 0.0 if ok else 1.0
+
+
+def _record_vector():
+    """One 128-channel vector with a known INT8 encoding, group by group:
+    group 0 at s = 1 (code 0x78), group 1 at s = 2 (0x80), group 2 at
+    s = 1.125 (0x79), group 3 at s = 0.5 (0x70); each group's largest
+    magnitude is exactly 127 * s, so its code is the one named."""
+    x = np.zeros(128)
+    x[0:4] = [127.0, -127.0, 3.0, -5.0]                 # -> 7F 81 03 FB
+    x[32:36] = [254.0, 14.0, -1.0, 3.0]                 # -> 7F 07 00 02 (-0.5, 1.5 are ties)
+    x[64:66] = [-127 * 1.125, 11.25]                    # -> 81 0A
+    x[96], x[127] = 63.5, -0.75                         # -> 7F FE
+    vbytes = np.zeros(128, dtype=np.uint8)
+    vbytes[0:4] = [0x7F, 0x81, 0x03, 0xFB]
+    vbytes[32:36] = [0x7F, 0x07, 0x00, 0x02]
+    vbytes[64:66] = [0x81, 0x0A]
+    vbytes[96], vbytes[127] = 0x7F, 0xFE
+    return x, vbytes, [0x78, 0x80, 0x79, 0x70]
+
+
+def pin_int8_record_bytes(Ox):
+    """Output and QKV INT8 records byte by byte, expected bytes written out
+    by hand (Sol-H3 section 3.2 "Quantized communication"; record layout as
+    read there): output record = 128 value bytes, the 4 group codes in
+    channel order at bytes 128-131, 12 zero bytes; QKV record = q, k, v value
+    bytes, then q's 4 codes, k's 4 codes, v's 4 codes (bytes 384-395), then
+    4 zero bytes.  k = 2x and v = x/2 keep every quotient (so the value
+    bytes) and move each code by one exponent step (+-8)."""
+    x, vbytes, codes = _record_vector()
+    o = Ox.out_int8_records(x[None, None, :])[0, 0]
+    want = np.zeros(144, dtype=np.uint8)
+    want[:128] = vbytes
+    want[128:132] = codes
+    worst = 0.0 if (o.shape == (144,) and np.array_equal(o, want)) else 1.0
+    r = Ox.qkv_int8_records(x[None, None, :], 2.0 * x[None, None, :], 0.5 * x[None, None, :])[0, 0]
+    want = np.zeros(400, dtype=np.uint8)
+    want[0:128] = want[128:256] = want[256:384] = vbytes
+    want[384:388] = codes
+    want[388:392] = [c + 8 for c in codes]
+    want[392:396] = [c - 8 for c in codes]
+    worst += 0.0 if (r.shape == (400,) and np.array_equal(r, want)) else 1.0
+    return worst
+
+
+def pin_block_sparse_empty_list(Ox):
+    """Sol-H3 section 3.4, "Safety rails and the exact prefix KV sink": with
+    no prefix a query block's list may be empty (a constant score row keeps
+    nothing above its mean); its rows then output exactly 0 (the reading
+    taken for a query with no key), while the other blocks attend normally."""
+    rng = np.random.default_rng(18)
+    B, n, H = 8, 30, 2
+    q, k, v = (rng.standard_normal((32, H, 128)) for _ in range(3))
+    nb = 4
+    keep = np.ones((H, nb, nb), bool)
+    keep[0, 1] = False                          # head 0, query block 1 (rows 8..15)
+    keep[1, 3] = False                          # head 1, the partial last block (rows 24..29)
+    got = Ox.block_sparse_attention(q, k, v, n, keep, B, 0.1)
+    dense = Ox.attention(q, k, v, [0, 32], [0, 32], [n], 0.1)
+    worst = 0.0 if (np.all(got[8:16, 0] == 0.0) and np.all(got[24:30, 1] == 0.0)) else 1.0
+    mask = np.ones((32, H), bool)
+    mask[8:16, 0] = mask[24:30, 1] = False
+    mask[n:] = False
+    worst += float(np.max(np.abs(got - dense)[mask]))
+    return worst
+
+
 def pin_softmax_rows(Ox):
     rng = np.random.default_rng(7)
     s = rng.standard_normal((9, 300)) * 40.0
@@ -455,6 +549,9 @@ PINS = [
     (pin_ue5m3_int8, 1e-12),
     (pin_e4m3, 0.0),
     (pin_wire_records, 0.0),
+    (pin_int8_ties_and_clamp, 0.0),
+    (pin_int8_record_bytes, 0.0),
+    (pin_block_sparse_empty_list, 1e-12),
     (pin_lora_prologue, 1e-12),
 ]
 
@@ -496,7 +593,8 @@ def _mutant(**overrides):
         s = ns.ue5m3_value(codes)[..., None]
         vals = np.clip(np.rint(g / s), -127, 127).astype(np.int8)
         return vals.reshape(x.shape), codes.astype(np.uint8)
-    ns.int8_group32 = int8_group32
+    if "int8_group32" not in overrides:
+        ns.int8_group32 = int8_group32
     ns.attention = attention
     return ns
 
@@ -632,6 +730,35 @@ def _lora_no_round(base, delta, w, pos, sections=SECTIONS, theta=THETA, eps=EPS)
     return O.qk_norm_rope(base + delta, w, pos, sections, theta, eps)
 
 
+def _int8_half_up(x):
+    g = x.reshape(x.shape[:-1] + (x.shape[-1] // 32, 32))
+    codes = O.ue5m3_scale_code(np.abs(g).max(axis=-1))
+    s = O.ue5m3_value(codes)[..., None]
+    vals = np.clip(np.floor(g / s + 0.5), -127, 127).astype(np.int8)
+    return vals.reshape(x.shape), codes.astype(np.uint8)
+
+
+def _int8_clip_asymmetric(x):
+    g = x.reshape(x.shape[:-1] + (x.shape[-1] // 32, 32))
+    codes = O.ue5m3_scale_code(np.abs(g).max(axis=-1))
+    s = O.ue5m3_value(codes)[..., None]
+    vals = np.clip(np.rint(g / s), -128, 127).astype(np.int8)
+    return vals.reshape(x.shape), codes.astype(np.uint8)
+
+
+def _out_codes_reversed(o):
+    rec = O.out_int8_records(o)
+    rec[..., 128:132] = rec[..., 128:132][..., ::-1].copy()
+    return rec
+
+
+def _sparse_empty_attends_all(q, k, v, n_rows, keep, block, scale, rows=None):
+    keep = keep.copy()
+    empty = ~keep.any(-1)
+    keep[empty] = True
+    return O.block_sparse_attention(q, k, v, n_rows, keep, block, scale, rows)
+
+
 MUTANTS = {
     "rope_sign_flip": dict(rope_axial=_rope_sign_flip),
     "rope_rotate_half": dict(rope_axial=_rope_rotate_half),
@@ -655,6 +782,10 @@ MUTANTS = {
     "scale_code_rounds_down": dict(ue5m3_scale_code=_scale_code_down),
     "e4m3_no_saturation": dict(e4m3_round=_e4m3_no_saturation),
     "pack_tensor_major": dict(pack_qkv=_pack_tensor_major),
+    "int8_rounds_half_up": dict(int8_group32=_int8_half_up),
+    "int8_clips_to_minus_128": dict(int8_group32=_int8_clip_asymmetric),
+    "out_record_codes_reversed": dict(out_int8_records=_out_codes_reversed),
+    "sparse_empty_list_attends_all": dict(block_sparse_attention=_sparse_empty_attends_all),
 }
 
 
@@ -710,3 +841,28 @@ def test_inputs_deterministic_and_padded():
     assert torch.isnan(c["k"][250:].float()).any() and torch.isinf(c["v"][250:].float()).any()
     assert torch.equal(a["q"][:250].view(torch.int16), c["q"][:250].view(torch.int16))
     assert torch.isnan(a["out"].float()).all()
+
+
+def test_attention_medium_against_sdpa():
+    """Library cross-check at the multi-tile size: the 4,000-valid-row,
+    42-head packed sequence (32 key tiles of 128 rows, a ragged last one),
+    prologue included, against torch SDPA in float64 on the CPU, head by
+    head over every valid row (the packed sequence and valid length of the
+    vLLM-Omni blog section 3.1)."""
+    inp = W.make_inputs("medium")
+    n = inp["valid_len"][0]
+    pos = inp["pos_thw"].numpy()[:n]
+    q = O.qk_norm_rope(O.widen(inp["q"][:n]), O.widen(inp["wq"]), pos, SECTIONS, THETA, EPS)
+    k = O.qk_norm_rope(O.widen(inp["k"][:n]), O.widen(inp["wk"]), pos, SECTIONS, THETA, EPS)
+    v = O.widen(inp["v"][:n])
+    pad = np.full((inp["q"].shape[0] - n,) + q.shape[1:], np.nan)
+    got = O.attention(np.concatenate([q, pad]), np.concatenate([k, pad]),
+                      np.concatenate([v, pad]), inp["cu_seqlens_q"], inp["cu_seqlens_kv"],
+                      inp["valid_len"], SCALE)
+    assert np.all(got[n:] == 0.0)
+    worst = 0.0
+    for h in range(q.shape[1]):
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a[:, h]))[None, None]
+        ref = torch.nn.functional.scaled_dot_product_attention(t(q), t(k), t(v), scale=SCALE)
+        worst = max(worst, float(np.max(np.abs(got[:n, h] - ref[0, 0].numpy()))))
+    assert worst <= 1e-12, worst
