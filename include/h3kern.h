@@ -15,10 +15,14 @@
  * (row_stride >= n_heads * 128), so that views into a packed
  * [rows, 3, n_heads, 128] QKV buffer can be passed without a copy.
  *
- * Errors: arguments are checked on the host before any CUDA call; a failed
- * check returns a negative status and launches nothing.  The library never
- * aborts or exits.  The message of the last nonzero status of the calling
- * thread is available from h3_last_error().
+ * Errors: arguments are checked on the host before any launch; a failed
+ * check returns a negative status and launches nothing.  Besides the checks
+ * each call lists, every pointer a kernel reads or writes is queried with
+ * cudaPointerGetAttributes and must be memory of the current device (or
+ * managed memory): host memory, pinned or not, and another GPU's memory are
+ * rejected with H3_ERR_ARG.  The library never aborts or exits.  The message
+ * of the last nonzero status of the calling thread is available from
+ * h3_last_error().
  */
 #ifndef H3KERN_H
 #define H3KERN_H
@@ -33,7 +37,8 @@ typedef struct CUstream_st* h3_stream_t; /* a cudaStream_t; NULL = legacy defaul
 
 enum {
   H3_OK = 0,
-  H3_ERR_ARG = -1,     /* null pointer, bad count, non-finite scalar, bad cu_seqlens */
+  H3_ERR_ARG = -1,     /* null or non-device pointer, bad count, non-finite scalar,
+                          bad cu_seqlens */
   H3_ERR_ALIGN = -2,   /* base pointer or row stride not 16-byte aligned */
   H3_ERR_SHAPE = -3,   /* head_dim != 128, row stride too small, bad rotary split */
   H3_ERR_ARCH = -4,    /* current device is not compute capability 10.3 (sm_103) */
@@ -216,9 +221,18 @@ int h3_attention_groups(const void* q, int64_t q_row_stride, const void* k, int6
  */
 
 /* x: device bf16 [n_rows, n_heads, 128] (row stride in elements, 16-byte
- * aligned); means: device fp32 [n_b, n_heads, 128], 4-byte aligned. */
+ * aligned); means: device fp32 [n_b, n_heads, 128], 4-byte aligned.  Each
+ * mean is an fp32 sum in a fixed order divided by the block's row count
+ * (deterministic run to run). */
 int h3_block_means(const void* x, int64_t row_stride, int64_t n_rows, int n_heads, int head_dim,
                    float* means, h3_stream_t stream);
+
+/* The block means of Q and of K in one launch: q -> q_means, k -> k_means,
+ * each as h3_block_means (same results bit for bit); the two means buffers
+ * must be distinct. */
+int h3_block_means_qk(const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,
+                      int64_t n_rows, int n_heads, int head_dim, float* q_means, float* k_means,
+                      h3_stream_t stream);
 
 /* q_means [n_q_blocks, n_heads, 128], k_means [n_kv_blocks, n_heads, 128]
  * (device fp32, 16-byte aligned; n_kv_blocks <= 2048).  Outputs (device,

@@ -14,7 +14,7 @@ strides and the current stream:
 * ``attention_groups`` -- query groups over KV views into the current K/V
   plus a cached K/V range (Sol-H3 reference KV caching, Fig. 4; SolarWM
   history K/V reuse).
-* ``block_means`` / ``block_select`` / ``sparse_attention`` (and
+* ``block_means`` (``block_means_qk``) / ``block_select`` / ``sparse_attention`` (and
   ``sol_attention`` chaining them) -- Sol-Attn block-sparse attention with
   the exact prefix KV sink (Sol-H3 section 3.4).
 * ``pack_qkv`` / ``unpack_qkv`` / ``pack_out`` / ``merge_heads`` -- the
@@ -35,7 +35,7 @@ import torch
 from . import _binding
 
 __all__ = ["H3Error", "qk_norm_rope", "qk_norm_rope_lora", "attention", "attention_groups",
-           "block_means", "block_select", "sparse_attention", "sol_attention",
+           "block_means", "block_means_qk", "block_select", "sparse_attention", "sol_attention",
            "WIRE_BF16", "WIRE_INT8", "WIRE_FP8", "wire_record_bytes", "pack_qkv", "unpack_qkv",
            "pack_out", "merge_heads",
            "status_word", "lib", "HEAD_DIM", "MAX_SEGMENTS", "attention_block",
@@ -60,7 +60,25 @@ def _check(status: int):
         raise H3Error(status, lib().h3_last_error().decode())
 
 
+def _on_device(t: torch.Tensor, name: str) -> torch.Tensor:
+    """Every pointer the kernels read or write must be memory of the current
+    CUDA device: a host tensor, or one on another GPU, would have its
+    address encoded into a tensor map or dereferenced in a kernel."""
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (got device {t.device})")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, but the current device is "
+                         f"cuda:{torch.cuda.current_device()}")
+    return t
+
+
+def _heads(t: torch.Tensor, name: str, n_heads: int) -> None:
+    if t.dim() < 2 or t.shape[1] != n_heads:
+        raise ValueError(f"{name} must have {n_heads} heads, got shape {tuple(t.shape)}")
+
+
 def _row_stride(t: torch.Tensor, name: str) -> int:
+    _on_device(t, name)
     if t.dtype != torch.bfloat16:
         raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
     if t.dim() != 3 or t.shape[-1] != HEAD_DIM:
@@ -85,15 +103,12 @@ def qk_norm_rope(q: torch.Tensor, k: torch.Tensor, wq: torch.Tensor, wk: torch.T
     """In place: q, k <- RoPE(RMSNorm(x) * w) for rows [0, n_rows)."""
     qs, ks = _row_stride(q, "q"), _row_stride(k, "k")
     H = q.shape[1]
+    _heads(k, "k", H)
     if n_rows is None:
         n_rows = q.shape[0]
     if not (0 <= n_rows <= min(q.shape[0], k.shape[0], pos_thw.shape[0])):
         raise ValueError("n_rows exceeds the tensors")
-    if pos_thw.dtype != torch.int32 or not pos_thw.is_contiguous() or pos_thw.shape[-1] != 3:
-        raise ValueError("pos_thw must be contiguous int32 [rows, 3]")
-    for w, name in ((wq, "wq"), (wk, "wk")):
-        if w.dtype != torch.bfloat16 or not w.is_contiguous() or tuple(w.shape) != (H, HEAD_DIM):
-            raise ValueError(f"{name} must be contiguous bf16 [{H}, {HEAD_DIM}]")
+    _prologue_small_inputs(wq, wk, pos_thw, H)
     _check(lib().h3_qk_norm_rope(q.data_ptr(), qs, k.data_ptr(), ks, wq.data_ptr(),
                                  wk.data_ptr(), pos_thw.data_ptr(), int(n_rows), H, HEAD_DIM,
                                  int(rot[0]), int(rot[1]), int(rot[2]), float(theta),
@@ -110,21 +125,29 @@ def qk_norm_rope_lora(q: torch.Tensor, q_delta: torch.Tensor, k: torch.Tensor,
     qs, ks = _row_stride(q, "q"), _row_stride(k, "k")
     dqs, dks = _row_stride(q_delta, "q_delta"), _row_stride(k_delta, "k_delta")
     H = q.shape[1]
+    for t, name in ((k, "k"), (q_delta, "q_delta"), (k_delta, "k_delta")):
+        _heads(t, name, H)
     if n_rows is None:
         n_rows = q.shape[0]
     if not (0 <= n_rows <= min(q.shape[0], k.shape[0], q_delta.shape[0], k_delta.shape[0],
                                pos_thw.shape[0])):
         raise ValueError("n_rows exceeds the tensors")
-    if pos_thw.dtype != torch.int32 or not pos_thw.is_contiguous() or pos_thw.shape[-1] != 3:
-        raise ValueError("pos_thw must be contiguous int32 [rows, 3]")
-    for w, name in ((wq, "wq"), (wk, "wk")):
-        if w.dtype != torch.bfloat16 or not w.is_contiguous() or tuple(w.shape) != (H, HEAD_DIM):
-            raise ValueError(f"{name} must be contiguous bf16 [{H}, {HEAD_DIM}]")
+    _prologue_small_inputs(wq, wk, pos_thw, H)
     _check(lib().h3_qk_norm_rope_lora(q.data_ptr(), qs, q_delta.data_ptr(), dqs, k.data_ptr(), ks,
                                       k_delta.data_ptr(), dks, wq.data_ptr(), wk.data_ptr(),
                                       pos_thw.data_ptr(), int(n_rows), H, HEAD_DIM, int(rot[0]),
                                       int(rot[1]), int(rot[2]), float(theta), float(eps),
                                       _stream(stream)))
+
+
+def _prologue_small_inputs(wq, wk, pos_thw, H):
+    _on_device(pos_thw, "pos_thw")
+    if pos_thw.dtype != torch.int32 or not pos_thw.is_contiguous() or pos_thw.shape[-1] != 3:
+        raise ValueError("pos_thw must be contiguous int32 [rows, 3]")
+    for w, name in ((wq, "wq"), (wk, "wk")):
+        _on_device(w, name)
+        if w.dtype != torch.bfloat16 or not w.is_contiguous() or tuple(w.shape) != (H, HEAD_DIM):
+            raise ValueError(f"{name} must be contiguous bf16 [{H}, {HEAD_DIM}]")
 
 
 def _i32_array(values: Sequence[int]):
@@ -143,6 +166,8 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     if out is None:
         out = torch.empty((q.shape[0], H, HEAD_DIM), dtype=torch.bfloat16, device=q.device)
     strides = [_row_stride(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"))]
+    for t, name in ((k, "k"), (v, "v"), (out, "out")):
+        _heads(t, name, H)
     n_seq = len(cu_seqlens_q) - 1
     if len(cu_seqlens_kv) != n_seq + 1 or (valid_len is not None and len(valid_len) != n_seq):
         raise ValueError("cu_seqlens_q, cu_seqlens_kv and valid_len disagree on n_seq")
@@ -179,6 +204,8 @@ def attention_groups(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, groups,
             raise ValueError("a group uses the cache but k_cache / v_cache are missing")
         tensors += [(k_cache, "k_cache"), (v_cache, "v_cache")]
     strides = {n: _row_stride(t, n) for t, n in tensors}
+    for t, name in tensors[1:]:
+        _heads(t, name, H)
     for (q0, nq, k0, nk, c0, nc) in groups:
         if q0 + nq > min(q.shape[0], out.shape[0]) or k0 + nk > min(k.shape[0], v.shape[0]) or \
                 (nc and c0 + nc > min(k_cache.shape[0], v_cache.shape[0])):
@@ -203,6 +230,8 @@ def block_means(x: torch.Tensor, n_rows: Optional[int] = None, stream=None) -> t
     """fp32 [ceil(n_rows / 128), H, 128]: mean of each 128-row block."""
     xs = _row_stride(x, "x")
     n_rows = x.shape[0] if n_rows is None else n_rows
+    if n_rows > x.shape[0]:
+        raise ValueError("n_rows exceeds the tensor")
     H = x.shape[1]
     out = torch.empty((-(-n_rows // BLOCK), H, HEAD_DIM), dtype=torch.float32, device=x.device)
     _check(lib().h3_block_means(x.data_ptr(), xs, int(n_rows), H, HEAD_DIM, out.data_ptr(),
@@ -210,12 +239,28 @@ def block_means(x: torch.Tensor, n_rows: Optional[int] = None, stream=None) -> t
     return out
 
 
+def block_means_qk(q: torch.Tensor, k: torch.Tensor, n_rows: Optional[int] = None, stream=None):
+    """(q_means, k_means), each fp32 [ceil(n_rows / 128), H, 128], in one launch."""
+    qs, ks = _row_stride(q, "q"), _row_stride(k, "k")
+    n_rows = q.shape[0] if n_rows is None else n_rows
+    H = q.shape[1]
+    _heads(k, "k", H)
+    if n_rows > min(q.shape[0], k.shape[0]):
+        raise ValueError("n_rows exceeds the tensors")
+    qm, km = (torch.empty((-(-n_rows // BLOCK), H, HEAD_DIM), dtype=torch.float32, device=q.device)
+              for _ in range(2))
+    _check(lib().h3_block_means_qk(q.data_ptr(), qs, k.data_ptr(), ks, int(n_rows), H, HEAD_DIM,
+                                   qm.data_ptr(), km.data_ptr(), _stream(stream)))
+    return qm, km
+
+
 def block_select(q_means: torch.Tensor, k_means: torch.Tensor, tau: float, n_prefix_blocks: int,
                  scale: Optional[float] = None, with_scores: bool = False, stream=None):
     """(lists int32 [H, nqb, nkb], counts int32 [H, nqb][, scores fp32])."""
     nqb, H, _ = q_means.shape
     nkb = k_means.shape[0]
-    for t in (q_means, k_means):
+    for t, name in ((q_means, "q_means"), (k_means, "k_means")):
+        _on_device(t, name)
         if t.dtype != torch.float32 or not t.is_contiguous() or t.shape[1:] != (H, HEAD_DIM):
             raise ValueError("means must be contiguous fp32 [n_blocks, H, 128]")
     if scale is None:
@@ -239,10 +284,16 @@ def sparse_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, lists: t
     if out is None:
         out = torch.empty((q.shape[0], H, HEAD_DIM), dtype=torch.bfloat16, device=q.device)
     strides = [_row_stride(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"))]
+    for t, name in ((k, "k"), (v, "v"), (out, "out")):
+        _heads(t, name, H)
+    _on_device(lists, "lists")
+    _on_device(counts, "counts")
     nb = -(-n_rows // BLOCK)
     if tuple(lists.shape) != (H, nb, nb) or tuple(counts.shape) != (H, nb) or \
             lists.dtype != torch.int32 or counts.dtype != torch.int32:
         raise ValueError("lists / counts do not match the sequence")
+    if not lists.is_contiguous() or not counts.is_contiguous():
+        raise ValueError("lists / counts must be contiguous")
     if n_rows > min(q.shape[0], k.shape[0], v.shape[0], out.shape[0]):
         raise ValueError("n_rows exceeds the tensors")
     if scale is None:
@@ -257,8 +308,7 @@ def sparse_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, lists: t
 def sol_attention(q, k, v, n_rows: int, tau: float, n_prefix_rows: int,
                   scale: Optional[float] = None, out=None, stream=None):
     """The three block-sparse stages in a row; returns (out, lists, counts)."""
-    qm = block_means(q, n_rows, stream)
-    km = block_means(k, n_rows, stream)
+    qm, km = block_means_qk(q, k, n_rows, stream)
     lists, counts = block_select(qm, km, tau, -(-n_prefix_rows // BLOCK), scale, stream=stream)
     out = sparse_attention(q, k, v, lists, counts, n_rows, scale, out, stream)
     return out, lists, counts
@@ -281,6 +331,10 @@ def pack_qkv(q, k, v, n_dest: int, fmt: int = WIRE_BF16, stream=None) -> torch.T
     rec = wire_record_bytes("qkv", fmt)
     wire = torch.empty((n_dest, rows, H // n_dest, rec), dtype=torch.uint8, device=q.device)
     s = [_row_stride(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"))]
+    for t, name in ((k, "k"), (v, "v")):
+        _heads(t, name, H)
+        if t.shape[0] < rows:
+            raise ValueError(f"{name} has fewer rows than q")
     _check(lib().h3_pack_qkv(q.data_ptr(), s[0], k.data_ptr(), s[1], v.data_ptr(), s[2], rows, H,
                              int(n_dest), int(fmt), wire.data_ptr(), _stream(stream)))
     return wire
@@ -289,6 +343,7 @@ def pack_qkv(q, k, v, n_dest: int, fmt: int = WIRE_BF16, stream=None) -> torch.T
 def unpack_qkv(wire: torch.Tensor, fmt: int = WIRE_BF16, stream=None):
     """wire [rows, heads, record] -> (q, k, v) bf16 [rows, heads, 128]."""
     rows, hl = wire.shape[0], wire.shape[1]
+    _on_device(wire, "wire")
     if not wire.is_contiguous() or wire.shape[2] != wire_record_bytes("qkv", fmt):
         raise ValueError("wire must be contiguous [rows, heads, record]")
     q, k, v = (torch.empty((rows, hl, HEAD_DIM), dtype=torch.bfloat16, device=wire.device)
@@ -312,11 +367,15 @@ def pack_out(out: torch.Tensor, fmt: int = WIRE_BF16, stream=None) -> torch.Tens
 def merge_heads(wire: torch.Tensor, fmt: int = WIRE_BF16, out=None, stream=None) -> torch.Tensor:
     """wire [n_src, rows, H/n_src, record] -> out bf16 [rows, H, 128]."""
     n_src, rows, hl = wire.shape[0], wire.shape[1], wire.shape[2]
+    _on_device(wire, "wire")
     if not wire.is_contiguous() or wire.shape[3] != wire_record_bytes("out", fmt):
         raise ValueError("wire must be contiguous [n_src, rows, heads, record]")
     H = n_src * hl
     if out is None:
         out = torch.empty((rows, H, HEAD_DIM), dtype=torch.bfloat16, device=wire.device)
+    _heads(out, "out", H)
+    if out.shape[0] < rows:
+        raise ValueError("out has fewer rows than the records")
     _check(lib().h3_merge_heads(wire.data_ptr(), rows, H, n_src, int(fmt), out.data_ptr(),
                                 _row_stride(out, "out"), _stream(stream)))
     return out

@@ -38,6 +38,8 @@ SIGNATURES = {
                                     c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_int64,
                                     c_void_p, c_int, c_int, c_int, c_float, c_void_p]),
     "h3_block_means": (c_int, [c_void_p, c_int64, c_int64, c_int, c_int, c_void_p, c_void_p]),
+    "h3_block_means_qk": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_int64, c_int, c_int,
+                                  c_void_p, c_void_p, c_void_p]),
     "h3_block_select": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_float, c_float, c_int,
                                 c_void_p, c_void_p, c_void_p, c_void_p]),
     "h3_sparse_attention": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_int64,

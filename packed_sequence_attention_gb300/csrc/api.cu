@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <initializer_list>
 #include <string>
 
 #include "h3_internal.h"
@@ -50,6 +51,38 @@ int check_device() {
   const bool ok = (major == 10 && minor == 3);
   if (dev >= 0 && dev < 64) cache[dev].store(ok ? 1 : 2);
   if (!ok) return fail(H3_ERR_ARCH, "device %d is sm_%d%d, the kernels need sm_103", dev, major, minor);
+  return H3_OK;
+}
+
+// Every pointer a kernel dereferences (or encodes into a tensor map) must be
+// memory of the current device, or managed memory: a host buffer or another
+// GPU's memory would otherwise reach the kernel as a bad address.  NULL
+// entries (optional outputs) are skipped.  Call after check_device().
+struct DevPtr {
+  const void* p;
+  const char* name;
+};
+
+int check_device_memory(std::initializer_list<DevPtr> ptrs) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(H3_ERR_DEVICE, "cudaGetDevice: %s", cudaGetErrorString(e));
+  for (const DevPtr& d : ptrs) {
+    if (d.p == nullptr) continue;
+    cudaPointerAttributes attr{};
+    e = cudaPointerGetAttributes(&attr, d.p);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();  // a failed query leaves no sticky error
+      return fail(H3_ERR_ARG, "%s: cannot query the pointer (%s)", d.name, cudaGetErrorString(e));
+    }
+    if (attr.type == cudaMemoryTypeManaged) continue;
+    if (attr.type != cudaMemoryTypeDevice)
+      return fail(H3_ERR_ARG, "%s is host memory; it must be memory of the current device %d",
+                  d.name, dev);
+    if (attr.device != dev)
+      return fail(H3_ERR_ARG, "%s is memory of device %d, but the current device is %d", d.name,
+                  attr.device, dev);
+  }
   return H3_OK;
 }
 
@@ -108,6 +141,9 @@ int norm_rope_entry(void* q, int64_t q_row_stride, void* k, int64_t k_row_stride
   if (n_rows > (int64_t(1) << 30))
     return fail(H3_ERR_SHAPE, "n_rows too large for one launch");
   int st = check_device();
+  if (st != H3_OK) return st;
+  st = check_device_memory({{q, "q"}, {k, "k"}, {wq, "wq"}, {wk, "wk"}, {pos_thw, "pos_thw"},
+                            {lora ? dq : nullptr, "q_delta"}, {lora ? dk : nullptr, "k_delta"}});
   if (st != H3_OK) return st;
   h3::NormRopeArgs a{};
   a.q = static_cast<__nv_bfloat16*>(q);
@@ -197,6 +233,8 @@ int h3_attention(const void* q, int64_t q_row_stride, const void* k, int64_t k_r
     return fail(H3_ERR_SHAPE, "row stride too large for a tensor map");
   int st = check_device();
   if (st != H3_OK) return st;
+  st = check_device_memory({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}});
+  if (st != H3_OK) return st;
   h3::AttnArgs a{};
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.k = static_cast<const __nv_bfloat16*>(k);
@@ -266,6 +304,10 @@ int h3_attention_groups(const void* q, int64_t q_row_stride, const void* k, int6
     return fail(H3_ERR_SHAPE, "row stride too large for a tensor map");
   int st = check_device();
   if (st != H3_OK) return st;
+  st = check_device_memory({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"},
+                            {uses_cache ? k_cache : nullptr, "k_cache"},
+                            {uses_cache ? v_cache : nullptr, "v_cache"}});
+  if (st != H3_OK) return st;
   h3::AttnGroupArgs a{};
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.k = static_cast<const __nv_bfloat16*>(k);
@@ -289,24 +331,69 @@ int h3_attention_groups(const void* q, int64_t q_row_stride, const void* k, int6
   return H3_OK;
 }
 
-int h3_block_means(const void* x, int64_t row_stride, int64_t n_rows, int n_heads, int head_dim,
-                   float* means, h3_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared checks of one tensor of a block-means call.
+int means_tensor(const void* x, int64_t row_stride, const float* means, int n_heads,
+                 const char* name) {
+  if (row_stride < static_cast<int64_t>(n_heads) * h3::kHeadDim)
+    return fail(H3_ERR_SHAPE, "%s row stride must be >= n_heads*128", name);
+  if (!x || !means) return fail(H3_ERR_ARG, "null pointer argument (%s)", name);
+  if (!aligned16(x) || (row_stride * 2) % 16)
+    return fail(H3_ERR_ALIGN, "%s and its row stride must be 16-byte aligned", name);
+  if ((reinterpret_cast<uintptr_t>(means) & 3u) != 0)
+    return fail(H3_ERR_ALIGN, "the means of %s must be 4-byte aligned", name);
+  return H3_OK;
+}
+
+int block_means_entry(const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,
+                      int64_t n_rows, int n_heads, int head_dim, float* q_means, float* k_means,
+                      int n_tensors, h3_stream_t stream) {
   if (n_rows < 1 || n_rows > int64_t(h3::kMaxSparseBlocks) * 128)
     return fail(H3_ERR_ARG, "n_rows must be in [1, %d] (got %lld)", h3::kMaxSparseBlocks * 128,
                 (long long)n_rows);
   if (n_heads < 1 || n_heads > 65535) return fail(H3_ERR_ARG, "n_heads out of range (%d)", n_heads);
   if (head_dim != h3::kHeadDim) return fail(H3_ERR_SHAPE, "head_dim must be 128 (got %d)", head_dim);
-  if (row_stride < static_cast<int64_t>(n_heads) * h3::kHeadDim)
-    return fail(H3_ERR_SHAPE, "row stride must be >= n_heads*128");
-  if (!x || !means) return fail(H3_ERR_ARG, "null pointer argument");
-  if (!aligned16(x) || (row_stride * 2) % 16) return fail(H3_ERR_ALIGN, "x and its row stride must be 16-byte aligned");
-  if ((reinterpret_cast<uintptr_t>(means) & 3u) != 0) return fail(H3_ERR_ALIGN, "means must be 4-byte aligned");
-  int st = check_device();
+  int st = means_tensor(q, q_row_stride, q_means, n_heads, n_tensors == 2 ? "q" : "x");
+  if (st == H3_OK && n_tensors == 2) st = means_tensor(k, k_row_stride, k_means, n_heads, "k");
   if (st != H3_OK) return st;
-  cudaError_t e = h3::launch_block_means(static_cast<const __nv_bfloat16*>(x), row_stride, n_rows,
-                                         n_heads, means, reinterpret_cast<cudaStream_t>(stream));
+  if (n_tensors == 2 && q_means == k_means)
+    return fail(H3_ERR_ARG, "q_means and k_means must be distinct buffers");
+  if ((st = check_device())) return st;
+  if ((st = check_device_memory({{q, "q"}, {q_means, "q_means"},
+                                 {n_tensors == 2 ? k : nullptr, "k"},
+                                 {n_tensors == 2 ? k_means : nullptr, "k_means"}})))
+    return st;
+  h3::MeansJob job{};
+  job.x[0] = static_cast<const __nv_bfloat16*>(q);
+  job.stride[0] = q_row_stride;
+  job.out[0] = q_means;
+  job.x[1] = static_cast<const __nv_bfloat16*>(k);
+  job.stride[1] = k_row_stride;
+  job.out[1] = k_means;
+  cudaError_t e = h3::launch_block_means(job, n_tensors, n_rows, n_heads,
+                                         reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(H3_ERR_LAUNCH, "block means launch: %s", cudaGetErrorString(e));
   return H3_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int h3_block_means(const void* x, int64_t row_stride, int64_t n_rows, int n_heads, int head_dim,
+                   float* means, h3_stream_t stream) {
+  return block_means_entry(x, row_stride, nullptr, 0, n_rows, n_heads, head_dim, means, nullptr,
+                           1, stream);
+}
+
+int h3_block_means_qk(const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,
+                      int64_t n_rows, int n_heads, int head_dim, float* q_means, float* k_means,
+                      h3_stream_t stream) {
+  return block_means_entry(q, q_row_stride, k, k_row_stride, n_rows, n_heads, head_dim, q_means,
+                           k_means, 2, stream);
 }
 
 int h3_block_select(const float* q_means, const float* k_means, int n_q_blocks, int n_kv_blocks,
@@ -326,6 +413,9 @@ int h3_block_select(const float* q_means, const float* k_means, int n_q_blocks, 
       (scores && (reinterpret_cast<uintptr_t>(scores) & 3u)))
     return fail(H3_ERR_ALIGN, "lists, counts and scores must be 4-byte aligned");
   int st = check_device();
+  if (st != H3_OK) return st;
+  st = check_device_memory({{q_means, "q_means"}, {k_means, "k_means"}, {scores, "scores"},
+                            {lists, "lists"}, {counts, "counts"}});
   if (st != H3_OK) return st;
   cudaError_t e = h3::launch_block_select(q_means, k_means, n_q_blocks, n_kv_blocks, n_heads, scale,
                                           tau, n_prefix_blocks, scores, lists, counts,
@@ -356,6 +446,9 @@ int h3_sparse_attention(const void* q, int64_t q_row_stride, const void* k, int6
   if ((reinterpret_cast<uintptr_t>(lists) & 3u) || (reinterpret_cast<uintptr_t>(counts) & 3u))
     return fail(H3_ERR_ALIGN, "lists and counts must be 4-byte aligned");
   int st = check_device();
+  if (st != H3_OK) return st;
+  st = check_device_memory({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}, {lists, "lists"},
+                            {counts, "counts"}});
   if (st != H3_OK) return st;
   h3::SparseAttnArgs a{};
   a.q = static_cast<const __nv_bfloat16*>(q);
@@ -425,6 +518,7 @@ int h3_pack_qkv(const void* q, int64_t q_row_stride, const void* k, int64_t k_ro
   if (!aligned16(wire)) return fail(H3_ERR_ALIGN, "wire must be 16-byte aligned");
   if (n_rows == 0) return H3_OK;
   if ((st = check_device())) return st;
+  if ((st = check_device_memory({{q, "q"}, {k, "k"}, {v, "v"}, {wire, "wire"}}))) return st;
   h3::WireQkvArgs a{};
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.k = static_cast<const __nv_bfloat16*>(k);
@@ -457,6 +551,7 @@ int h3_unpack_qkv(const void* wire, int64_t n_rows, int n_heads_local, int forma
   if (!aligned16(wire)) return fail(H3_ERR_ALIGN, "wire must be 16-byte aligned");
   if (n_rows == 0) return H3_OK;
   if ((st = check_device())) return st;
+  if ((st = check_device_memory({{wire, "wire"}, {q, "q"}, {k, "k"}, {v, "v"}}))) return st;
   h3::WireQkvArgs a{};
   a.qm = static_cast<__nv_bfloat16*>(q);
   a.km = static_cast<__nv_bfloat16*>(k);
@@ -486,6 +581,7 @@ int h3_pack_out(const void* out, int64_t out_row_stride, int64_t n_rows, int n_h
   if (!aligned16(wire)) return fail(H3_ERR_ALIGN, "wire must be 16-byte aligned");
   if (n_rows == 0) return H3_OK;
   if ((st = check_device())) return st;
+  if ((st = check_device_memory({{out, "out"}, {wire, "wire"}}))) return st;
   h3::WireOutArgs a{};
   a.out = static_cast<const __nv_bfloat16*>(out);
   a.os = out_row_stride;
@@ -511,6 +607,7 @@ int h3_merge_heads(const void* wire, int64_t n_rows, int n_heads, int n_src, int
   if (!aligned16(wire)) return fail(H3_ERR_ALIGN, "wire must be 16-byte aligned");
   if (n_rows == 0) return H3_OK;
   if ((st = check_device())) return st;
+  if ((st = check_device_memory({{wire, "wire"}, {out, "out"}}))) return st;
   h3::WireOutArgs a{};
   a.outm = static_cast<__nv_bfloat16*>(out);
   a.os = out_row_stride;

@@ -19,33 +19,60 @@ namespace {
 
 constexpr int kBlk = 128;
 
-// grid (n_blocks, n_heads), 128 threads: 16 chunks of 8 channels x 8 row slices.
-__global__ void __launch_bounds__(128) block_means_kernel(const __nv_bfloat16* __restrict__ x,
-                                                          int64_t stride, int64_t n_rows, int H,
-                                                          float* __restrict__ out) {
+__device__ __forceinline__ uint4 ld_stream16(const uint4* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void add8(float* acc, const uint4 v) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc[2 * i] += __uint_as_float(u[i] << 16);
+    acc[2 * i + 1] += __uint_as_float(u[i] & 0xFFFF0000u);
+  }
+}
+
+// grid (n_heads, n_blocks, n_tensors), 128 threads: 16 chunks of 8 channels
+// x 8 row slices.  Consecutive CTAs take consecutive heads of the same
+// block, so the CTAs running together read whole rows between them.  A
+// thread sums rows slice, slice + 8, ... of its chunk in that order, then
+// the 8 slices are added in order: a fixed summation order, so the means
+// are deterministic.  A full block issues all 16 of a thread's loads before
+// the first add.
+__global__ void __launch_bounds__(128) block_means_kernel(MeansJob job, int64_t n_rows, int H) {
   __shared__ float red[8][kHeadDim];
-  const int b = blockIdx.x, h = blockIdx.y;
+  const int h = blockIdx.x, b = blockIdx.y;
+  const bool second = blockIdx.z != 0;
+  const __nv_bfloat16* x = second ? job.x[1] : job.x[0];
+  const int64_t stride = second ? job.stride[1] : job.stride[0];
+  float* out = second ? job.out[1] : job.out[0];
   const int chunk = threadIdx.x & 15, slice = threadIdx.x >> 4;
   const int64_t r0 = static_cast<int64_t>(b) * kBlk;
   const int rows = static_cast<int>(n_rows - r0 < kBlk ? n_rows - r0 : kBlk);
+  const uint4* src = reinterpret_cast<const uint4*>(x + (r0 + slice) * stride + h * kHeadDim) + chunk;
+  const int64_t step = stride;  // 8 rows apart, in 16-byte units: 8 * stride * 2 B / 16 B
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int r = slice; r < rows; r += 8) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (r0 + r) * stride + h * kHeadDim) + chunk);
-    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+  if (rows == kBlk) {
+    uint4 v[kBlk / 8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      acc[2 * i] += __uint_as_float(u[i] << 16);
-      acc[2 * i + 1] += __uint_as_float(u[i] & 0xFFFF0000u);
-    }
+    for (int i = 0; i < kBlk / 8; ++i) v[i] = ld_stream16(src + i * step);
+#pragma unroll
+    for (int i = 0; i < kBlk / 8; ++i) add8(acc, v[i]);
+  } else {
+    for (int r = slice, i = 0; r < rows; r += 8, ++i) add8(acc, ld_stream16(src + i * step));
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i) red[slice][chunk * 8 + i] = acc[i];
   __syncthreads();
   const int c = threadIdx.x;
-  float s = 0.f;
+  float sum = 0.f;
 #pragma unroll
-  for (int k = 0; k < 8; ++k) s += red[k][c];
-  out[(static_cast<int64_t>(b) * H + h) * kHeadDim + c] = s / static_cast<float>(rows);
+  for (int k = 0; k < 8; ++k) sum += red[k][c];
+  out[(static_cast<int64_t>(b) * H + h) * kHeadDim + c] = sum / static_cast<float>(rows);
 }
 
 constexpr int kSelThreads = 256;
@@ -124,10 +151,10 @@ __global__ void __launch_bounds__(kSelThreads) block_select_kernel(
 
 }  // namespace
 
-cudaError_t launch_block_means(const __nv_bfloat16* x, int64_t stride, int64_t n_rows, int H,
-                               float* out, cudaStream_t stream) {
+cudaError_t launch_block_means(const MeansJob& job, int n_tensors, int64_t n_rows, int H,
+                               cudaStream_t stream) {
   const int nb = static_cast<int>((n_rows + kBlk - 1) / kBlk);
-  block_means_kernel<<<dim3(nb, H), 128, 0, stream>>>(x, stride, n_rows, H, out);
+  block_means_kernel<<<dim3(H, nb, n_tensors), 128, 0, stream>>>(job, n_rows, H);
   return cudaGetLastError();
 }
 

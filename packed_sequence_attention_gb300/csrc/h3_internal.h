@@ -71,8 +71,14 @@ struct AttnGroupArgs {
 int launch_attention_groups(const AttnGroupArgs& a, cudaStream_t stream, std::string& err);
 
 // ------------------------------------------------------------ block sparse
-cudaError_t launch_block_means(const __nv_bfloat16* x, int64_t stride, int64_t n_rows, int H,
-                               float* out, cudaStream_t stream);
+// Block means of one or two tensors (x[0] -> out[0], x[1] -> out[1]) in one launch.
+struct MeansJob {
+  const __nv_bfloat16* x[2];
+  int64_t stride[2];  // elements
+  float* out[2];
+};
+cudaError_t launch_block_means(const MeansJob& job, int n_tensors, int64_t n_rows, int H,
+                               cudaStream_t stream);
 cudaError_t launch_block_select(const float* qm, const float* km, int nqb, int nkb, int H,
                                 float scale, float tau, int n_prefix, float* scores,
                                 int32_t* lists, int32_t* counts, cudaStream_t stream);

@@ -161,6 +161,18 @@ def test_block_means_rejects_on_host(lib, args, code):
 
 
 @pytest.mark.parametrize("args,code", [
+    (dict(n=0), ARG), (dict(n=2048 * 128 + 1), ARG), (dict(D=64), SHAPE), (dict(k=None), ARG),
+    (dict(km=None), ARG), (dict(k=A + 8), ALIGN), (dict(km=A + 2), ALIGN), (dict(ks=100), SHAPE),
+    (dict(qs=5380), ALIGN), (dict(km=A), ARG), (dict(H=0), ARG),
+])
+def test_block_means_qk_rejects_on_host(lib, args, code):
+    a = dict(q=A, qs=5376, k=A + 0x100000, ks=5376, n=1000, H=42, D=128, qm=A, km=A + 0x200000)
+    a.update(args)
+    assert lib.h3_block_means_qk(a["q"], a["qs"], a["k"], a["ks"], a["n"], a["H"], a["D"],
+                                 a["qm"], a["km"], None) == code
+
+
+@pytest.mark.parametrize("args,code", [
     (dict(nkb=2049), ARG), (dict(nqb=0), ARG), (dict(tau=float("inf")), ARG),
     (dict(npre=9), ARG), (dict(npre=-1), ARG), (dict(lists=None), ARG), (dict(qm=A + 4), ALIGN),
     (dict(counts=A + 2), ALIGN),

@@ -114,6 +114,9 @@ def test_block_sparse_stages():
     gm = [Guarded(nb * H * 128 * 4) for _ in range(2)]
     for g, x in zip(gm, (q, k)):
         assert lib.h3_block_means(x.data_ptr(), H * 128, rows, H, 128, g.ptr(), None) == 0
+    gqk = [Guarded(nb * H * 128 * 4) for _ in range(2)]
+    assert lib.h3_block_means_qk(q.data_ptr(), H * 128, k.data_ptr(), H * 128, rows, H, 128,
+                                 gqk[0].ptr(), gqk[1].ptr(), None) == 0
     gl, gc, gs = Guarded(H * nb * nb * 4), Guarded(H * nb * 4), Guarded(H * nb * nb * 4)
     assert lib.h3_block_select(gm[0].ptr(), gm[1].ptr(), nb, nb, H, SCALE, 0.5, 1, gs.ptr(),
                                gl.ptr(), gc.ptr(), None) == 0
@@ -122,7 +125,7 @@ def test_block_sparse_stages():
                                    H * 128, out.data_ptr(), out.stride(0), rows, H, 128, gl.ptr(),
                                    gc.ptr(), SCALE, None) == 0
     torch.cuda.synchronize()
-    assert all(g.margins_intact() for g in (*gm, gl, gc, gs)) and ok()
+    assert all(g.margins_intact() for g in (*gm, *gqk, gl, gc, gs)) and ok()
 
 
 @pytest.mark.parametrize("fmt", [h3.WIRE_BF16, h3.WIRE_INT8])
