@@ -651,30 +651,33 @@ def sol_attention_one(h3, g, w, stream, pk, tau=1.0, iters=5):
     s = w.segments[0]
     n = s.n_valid_q()
     q, k, v = g["q"], g["k"], g["v"]
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
 
-    def run(record):
-        if record:
+    def run(ev=None):
+        if ev is not None:
             ev[0].record(stream)
         qm, km = h3.block_means_qk(q, k, n)
-        if record:
+        if ev is not None:
             ev[1].record(stream)
         lists, counts = h3.block_select(qm, km, tau, -(-2310 // 128), SCALE)
-        if record:
+        if ev is not None:
             ev[2].record(stream)
         h3.sparse_attention(q, k, v, lists, counts, n, SCALE, out=g["out"])
-        if record:
+        if ev is not None:
             ev[3].record(stream)
         return counts
 
-    counts = run(False)
+    counts = run()
     torch.cuda.synchronize()
-    t = np.zeros(3)
-    for _ in range(iters):
-        run(True)
-        torch.cuda.synchronize()
-        t += [ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2]), ev[2].elapsed_time(ev[3])]
-    t /= iters
+    # Iterations are queued back to back, so that the host's launch work for
+    # one stage overlaps the GPU's previous work; the first iteration (queued
+    # on an idle stream, its start event firing before its first launch) is
+    # not counted.
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(iters + 1)]
+    for ev in evs:
+        run(ev)
+    torch.cuda.synchronize()
+    t = np.mean([[ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2]), ev[2].elapsed_time(ev[3])]
+                 for ev in evs[1:]], axis=0)
     nb = -(-n // 128)
     kept = float(counts.double().sum().item()) / (w.n_heads * nb * nb)
     flops_kept = kept * 4.0 * w.n_heads * 128 * n * n  # the first sequence only

@@ -286,7 +286,9 @@ int h3_wire_record_bytes(int what, int format);
 
 /* q, k, v [n_rows, n_heads, 128] (own row strides) -> wire
  * [n_dest][n_rows][n_heads / n_dest] QKV records, destination d holding heads
- * d * n_heads / n_dest ...; n_dest divides n_heads.  Format BF16 or INT8. */
+ * d * n_heads / n_dest ...; n_dest divides n_heads.  Format BF16 or INT8;
+ * INT8 needs q, k, v and their row strides 16-byte aligned (H3_ERR_ALIGN
+ * otherwise). */
 int h3_pack_qkv(const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,
                 const void* v, int64_t v_row_stride, int64_t n_rows, int n_heads, int n_dest,
                 int format, void* wire, h3_stream_t stream);

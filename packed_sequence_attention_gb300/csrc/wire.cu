@@ -221,132 +221,133 @@ __global__ void __launch_bounds__(kWarps * 32) pack_qkv_bf16_kernel(
 }
 
 // Block-INT8 QKV records.  Quantising costs more issue slots than the bytes
-// take to move, so the kernel is persistent and software-pipelined: a warp
-// loads its next pass (kU units) before it quantises the current one, and it
-// steps its unit indices without divisions (those cost ~10 % of the time).
-constexpr int kInt8PackU = 2;
+// take to move, so the layout is chosen to share work: a half-warp handles
+// one (token, head) unit, lane l owning channels 8 (l & 15) .. + 7 of each of
+// q, k and v (16-byte loads), so the 4 lanes of a 32-channel group reduce its
+// max with two xor-shuffles and lane j < 3 of the group derives the scale
+// code of tensor j once for the whole group.  The kernel is persistent and
+// software-pipelined: a warp loads its next pair of units before it
+// quantises the current one, and steps its unit indices without divisions.
+constexpr int kInt8Warps = 8;
 
-__global__ void __launch_bounds__(kWarps * 32) pack_qkv_int8_kernel(
+// 8 values of one tensor -> 8 int8 (two words), scale s, reciprocal r.
+__device__ __forceinline__ uint2 quant8(const float* x, float s, float r) {
+  return make_uint2(quant4(x, s, r), quant4(x + 4, s, r));
+}
+
+__device__ __forceinline__ void unpack8(const uint4 u, float* f) {
+  unpack4(make_uint2(u.x, u.y), f);
+  unpack4(make_uint2(u.z, u.w), f + 4);
+}
+
+__global__ void __launch_bounds__(kInt8Warps * 32, 4) pack_qkv_int8_kernel(
     const __nv_bfloat16* __restrict__ q, int64_t qs, const __nv_bfloat16* __restrict__ k, int64_t ks,
     const __nv_bfloat16* __restrict__ v, int64_t vs, int64_t n_rows, int H, int n_dest,
     uint8_t* __restrict__ wire) {
-  constexpr int kU = kInt8PackU;
   constexpr int kRec = 400;
   const int lane = threadIdx.x & 31;
+  const int half = lane >> 4, l16 = lane & 15;
+  const int j = lane & 3;               // lane within its 32-channel group
+  const int grp = l16 >> 2;             // the group (0..3) of this lane's channels
   const int hl = H / n_dest;
   const uint32_t total = static_cast<uint32_t>(n_rows * H);  // < 2^31, checked on the host
-  const uint32_t stride = gridDim.x * kWarps;
-  // A warp's first unit of pass p is u0 = p kU = row H + d hl + hloc.  The
-  // next pass is `stride` passes on: u0 grows by stride kU = drow H + dd hl +
-  // dh, so (row, d, hloc) advance by constants with carries, no division.
-  const uint32_t adv = stride * kU;
+  // 8 / (8 + m), correctly rounded, for m = lane & 7: 1 / value(c) is this
+  // times 2^(15 - (c >> 3)), with m = c & 7 (exact scaling by a power of 2).
+  const float recip_tbl = __fdiv_rn(8.0f, static_cast<float>(8 + (lane & 7)));
+  // This lane's unit of pass p is u = (p * 2) + half = row H + d hl + hloc.
+  // The next pass is `stride` passes on: u grows by adv = stride * 2 = drow H
+  // + dd hl + dh, so (row, d, hloc) advance by constants with carries.
+  const uint32_t stride = gridDim.x * kInt8Warps;
+  const uint32_t adv = stride * 2;
   const uint32_t drow = adv / static_cast<uint32_t>(H);
   const uint32_t rem = adv - drow * static_cast<uint32_t>(H);
   const int dd = static_cast<int>(rem) / hl, dh = static_cast<int>(rem) - dd * hl;
-  uint32_t u0 = (blockIdx.x * kWarps + (threadIdx.x >> 5)) * kU;
-  int64_t row = u0 / static_cast<uint32_t>(H);
-  int d0, hloc0;
+  uint32_t u = (blockIdx.x * kInt8Warps + (threadIdx.x >> 5)) * 2 + half;
+  int64_t row = u / static_cast<uint32_t>(H);
+  int d, hloc;
   {
-    const int head = static_cast<int>(u0 - static_cast<uint32_t>(row) * static_cast<uint32_t>(H));
-    d0 = head / hl;
-    hloc0 = head - d0 * hl;
+    const int head = static_cast<int>(u - static_cast<uint32_t>(row) * static_cast<uint32_t>(H));
+    d = head / hl;
+    hloc = head - d * hl;
   }
-  // Units of a pass starting at (row, d, hloc): unit u is (row_u, head_u), its record
-  // goes to destination d_u at local head hloc_u.
-  struct Pass {
-    int64_t r[kU];
-    int d[kU], hl_[kU];
-    bool ok[kU];
-  };
-  auto make_pass = [&](uint32_t base, int64_t r0, int dd0, int hh0) {
-    Pass ps;
-    int64_t r = r0;
-    int dx = dd0, hx = hh0;
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      ps.r[u] = r;
-      ps.d[u] = dx;
-      ps.hl_[u] = hx;
-      ps.ok[u] = base + u < total;
-      if (++hx == hl) {
-        hx = 0;
-        if (++dx == n_dest) {
-          dx = 0;
-          ++r;
-        }
-      }
-    }
-    return ps;
-  };
-  auto load = [&](const Pass& ps, uint2 (&in)[kU][3]) {
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      if (ps.ok[u]) {
-        const int64_t c = (ps.d[u] * hl + ps.hl_[u]) * kHeadDim + lane * 4;
-        in[u][0] = ld8(q + ps.r[u] * qs + c);
-        in[u][1] = ld8(k + ps.r[u] * ks + c);
-        in[u][2] = ld8(v + ps.r[u] * vs + c);
-      }
+  const int c8 = l16 * 8;
+  auto load = [&](uint32_t uu, int64_t r, int dx, int hx, uint4 (&in)[3]) {
+    if (uu < total) {
+      const int64_t c = static_cast<int64_t>(dx * hl + hx) * kHeadDim + c8;
+      in[0] = __ldg(reinterpret_cast<const uint4*>(q + r * qs + c));
+      in[1] = __ldg(reinterpret_cast<const uint4*>(k + r * ks + c));
+      in[2] = __ldg(reinterpret_cast<const uint4*>(v + r * vs + c));
+    } else {
+      in[0] = in[1] = in[2] = make_uint4(0u, 0u, 0u, 0u);
     }
   };
-  Pass cur = make_pass(u0, row, d0, hloc0);
-  uint2 in[kU][3] = {};
-  load(cur, in);
-  while (u0 < total) {
-    // next pass: advance (row, d0, hloc0) by (drow, dd, dh) with carries
-    const uint32_t nu0 = u0 + adv;
-    hloc0 += dh;
-    int carry = 0;
-    if (hloc0 >= hl) {
-      hloc0 -= hl;
-      carry = 1;
+  uint4 in[3];
+  load(u, row, d, hloc, in);
+  // Whole warps leave together: the pass loop runs while either half has a unit.
+  while (__any_sync(0xffffffffu, u < total)) {
+    const uint32_t nu = u + adv;
+    int64_t nrow = row + drow;
+    int nd = d + dd, nh = hloc + dh;
+    if (nh >= hl) {
+      nh -= hl;
+      ++nd;
     }
-    d0 += dd + carry;
-    row += drow;
-    if (d0 >= n_dest) {
-      d0 -= n_dest;
-      ++row;
+    if (nd >= n_dest) {
+      nd -= n_dest;
+      ++nrow;
     }
-    const Pass nx = make_pass(nu0, row, d0, hloc0);
-    uint2 nin[kU][3] = {};
-    if (nu0 < total) load(nx, nin);
-    // items i = 3u + t: unit u, tensor t; scale codes of all 3 kU items at once
-    float f[3 * kU][4], amax[3 * kU], s[3 * kU], rs[3 * kU];
+    uint4 nin[3];
+    load(nu, nrow, nd, nh, nin);
+    // this lane's 8 values of each tensor and the group maxima
+    float f[3][8], amax[3];
 #pragma unroll
-    for (int i = 0; i < 3 * kU; ++i) {
-      unpack4(in[i / 3][i % 3], f[i]);
-      amax[i] = group_amax(f[i]);
+    for (int t = 0; t < 3; ++t) {
+      unpack8(in[t], f[t]);
+      float a = fmax3(fabsf(f[t][0]), fabsf(f[t][1]), fabsf(f[t][2]));
+      a = fmax3(a, fabsf(f[t][3]), fabsf(f[t][4]));
+      a = fmax3(a, fabsf(f[t][5]), fabsf(f[t][6]));
+      a = fmaxf(a, fabsf(f[t][7]));
+      a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+      amax[t] = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
     }
-    bool sat;
-    const int code = group_scales<3 * kU>(amax, s, rs, &sat);
+    // lane j < 3 of each group: the code of tensor j; then s and 1/s of all
+    // three tensors for every lane of the group
+    const float a = j == 0 ? amax[0] : (j == 1 ? amax[1] : amax[2]);
+    const int code = ue5m3_code(a);
+    const float sc = ue5m3_value(code);
+    const float rc = __uint_as_float(
+        __float_as_uint(__shfl_sync(0xffffffffu, recip_tbl, code & 7)) +
+        (static_cast<uint32_t>(15 - (code >> 3)) << 23));
+    const bool sat = __any_sync(0xffffffffu, j < 3 && a > 127.0f * sc);
+    float s[3], r[3];
+#pragma unroll
+    for (int t = 0; t < 3; ++t) {
+      s[t] = __shfl_sync(0xffffffffu, sc, (lane & ~3) | t);
+      r[t] = __shfl_sync(0xffffffffu, rc, (lane & ~3) | t);
+    }
     if (sat) {
 #pragma unroll
-      for (int i = 0; i < 3 * kU; ++i) clamp4(f[i], s[i]);
+      for (int t = 0; t < 3; ++t) {
+        clamp4(f[t], s[t]);
+        clamp4(f[t] + 4, s[t]);
+      }
     }
-    uint8_t* dst[kU];
+    if (u < total) {
+      uint8_t* dst = wire + ((static_cast<int64_t>(d) * n_rows + row) * hl + hloc) * kRec;
 #pragma unroll
-    for (int u = 0; u < kU; ++u)
-      dst[u] = wire + ((static_cast<int64_t>(cur.d[u]) * n_rows + cur.r[u]) * hl + cur.hl_[u]) * kRec;
-#pragma unroll
-    for (int i = 0; i < 3 * kU; ++i)
-      if (cur.ok[i / 3])
-        *reinterpret_cast<uint32_t*>(dst[i / 3] + (i % 3) * 128 + lane * 4) = quant4(f[i], s[i], rs[i]);
-    // lane (g, j) holds the code of item j, group g; lane u < kU clears the
-    // pad word of unit u.  Pointers are picked by unrolled compares so that
-    // dst[] stays in registers.
-    const int j = lane & 7, g = lane >> 3;
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      if (!cur.ok[u]) break;
-      if (j / 3 == u && j < 3 * kU) dst[u][384 + (j - 3 * u) * 4 + g] = static_cast<uint8_t>(code);
-      if (lane == u) *reinterpret_cast<uint32_t*>(dst[u] + 396) = 0u;
+      for (int t = 0; t < 3; ++t)
+        *reinterpret_cast<uint2*>(dst + t * 128 + c8) = quant8(f[t], s[t], r[t]);
+      // codes: tensor j, group grp at byte 384 + 4 j + grp; lane 15 of the
+      // half clears the 4 pad bytes
+      if (j < 3) dst[384 + 4 * j + grp] = static_cast<uint8_t>(code);
+      if (l16 == 15) *reinterpret_cast<uint32_t*>(dst + 396) = 0u;
     }
-    cur = nx;
+    u = nu;
+    row = nrow;
+    d = nd;
+    hloc = nh;
 #pragma unroll
-    for (int u = 0; u < kU; ++u)
-#pragma unroll
-      for (int t = 0; t < 3; ++t) in[u][t] = nin[u][t];
-    u0 = nu0;
+    for (int t = 0; t < 3; ++t) in[t] = nin[t];
   }
 }
 
@@ -507,17 +508,19 @@ cudaError_t launch_pack_qkv(const WireQkvArgs& a, cudaStream_t s) {
   int64_t full = full_cache[dev].load();
   if (full == 0) {
     int per_sm = 0, sms = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pack_qkv_int8_kernel, kWarps * 32, 0);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pack_qkv_int8_kernel,
+                                                      kInt8Warps * 32, 0);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     full = static_cast<int64_t>(sms) * (per_sm < 1 ? 1 : per_sm);
     full_cache[dev].store(full);
   }
-  const int64_t need = blocks_for(a.n_rows * a.n_heads, kInt8PackU);
+  const int64_t units = a.n_rows * a.n_heads;
+  const int64_t need = (units + kInt8Warps * 2 - 1) / (kInt8Warps * 2);
   const unsigned g = static_cast<unsigned>(need < full ? need : full);
-  pack_qkv_int8_kernel<<<g, kWarps * 32, 0, s>>>(a.q, a.qs, a.k, a.ks, a.v, a.vs, a.n_rows,
-                                                 a.n_heads, a.n_parts, a.wire);
+  pack_qkv_int8_kernel<<<g, kInt8Warps * 32, 0, s>>>(a.q, a.qs, a.k, a.ks, a.v, a.vs, a.n_rows,
+                                                     a.n_heads, a.n_parts, a.wire);
   return cudaGetLastError();
 }
 

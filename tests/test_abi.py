@@ -206,12 +206,20 @@ def test_wire_record_sizes_on_host(lib):
     (dict(nd=4), ARG), (dict(nd=0), ARG), (dict(fmt=2), ARG), (dict(q=None), ARG),
     (dict(q=A + 4), ALIGN), (dict(ks=5375), SHAPE), (dict(wire=A + 8), ALIGN), (dict(H=0), ARG),
     (dict(n=2 ** 33), ARG), (dict(n=-1), ARG),
+    (dict(v=A + 8), ALIGN), (dict(qs=5376 + 4), ALIGN),          # INT8: 16-byte vectors
 ])
 def test_pack_qkv_rejects_on_host(lib, args, code):
     a = dict(q=A, qs=5376, k=A, ks=5376, v=A, vs=5376, n=10, H=42, nd=2, fmt=1, wire=A)
     a.update(args)
     assert lib.h3_pack_qkv(a["q"], a["qs"], a["k"], a["ks"], a["v"], a["vs"], a["n"], a["H"],
                            a["nd"], a["fmt"], a["wire"], None) == code
+
+
+def test_pack_qkv_bf16_allows_8_byte_alignment(lib):
+    """BF16 records move 8-byte vectors: an 8-byte aligned view passes the host
+    checks (and, without a GPU, stops at the device check)."""
+    st = lib.h3_pack_qkv(A + 8, 5376 + 4, A, 5376, A, 5376, 10, 42, 2, 0, A, None)
+    assert st in (DEVICE, ARCH) or (torch.cuda.is_available() and st == ARG)
 
 
 @pytest.mark.parametrize("args,code", [

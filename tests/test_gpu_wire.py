@@ -50,9 +50,12 @@ def test_pack_qkv_bf16_is_the_permutation(n_dest):
             assert torch.equal(a.view(torch.int16), b[:, hs].contiguous().view(torch.int16))
 
 
-@pytest.mark.parametrize("n_dest", [1, 2])
-def test_pack_qkv_int8_records_and_decode(n_dest):
-    q, k, v = qkv(packed=False, seed=1)
+@pytest.mark.parametrize("n_dest,rows,H", [(1, 300, 6), (2, 300, 6), (3, 301, 6), (1, 301, 5),
+                                           (5, 77, 5)])
+def test_pack_qkv_int8_records_and_decode(n_dest, rows, H):
+    # odd rows x heads leaves the last warp pass half full; hl odd makes a
+    # warp's two units straddle destinations
+    q, k, v = qkv(rows=rows, H=H, packed=False, seed=1)
     q[0, 0] = 0.0                     # an all-zero group
     k[1, 2, :32] *= 1000.0            # a wide group
     wire = h3.pack_qkv(q, k, v, n_dest, h3.WIRE_INT8)
