@@ -661,7 +661,8 @@ def sol_attention_one(h3, g, w, stream, pk, tau=1.0, iters=5):
         lists, counts = h3.block_select(qm, km, tau, -(-2310 // 128), SCALE)
         if ev is not None:
             ev[2].record(stream)
-        h3.sparse_attention(q, k, v, lists, counts, n, SCALE, out=g["out"])
+        h3.sparse_attention(q, k, v, lists, counts, n, SCALE, out=g["out"],
+                            n_prefix_blocks=-(-2310 // 128))
         if ev is not None:
             ev[3].record(stream)
         return counts

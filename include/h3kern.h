@@ -249,11 +249,16 @@ int h3_block_select(const float* q_means, const float* k_means, int n_q_blocks, 
  * lists / counts as h3_block_select writes them for this sequence
  * (n_q_blocks = n_kv_blocks = n_b).  Rows of a query block that keeps no
  * block are written as 0; rows >= n_rows are not written.  List entries
- * outside [0, n_b) are ignored. */
+ * outside [0, n_b) are ignored.
+ * n_prefix_blocks (0 .. n_b) is a scheduling hint, the value given to
+ * h3_block_select: the prefix query blocks keep every KV block, so their
+ * tiles take several times longer than the others and are scheduled first.
+ * It never changes the output (0 = no hint). */
 int h3_sparse_attention(const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,
                         const void* v, int64_t v_row_stride, void* out, int64_t out_row_stride,
                         int64_t n_rows, int n_heads, int head_dim, const int32_t* lists,
-                        const int32_t* counts, float scale, h3_stream_t stream);
+                        const int32_t* counts, int n_prefix_blocks, float scale,
+                        h3_stream_t stream);
 
 /*
  * Wire formats at the attention boundary (Sol-H3, section 3.2 "Optimized

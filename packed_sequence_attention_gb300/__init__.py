@@ -278,8 +278,12 @@ def block_select(q_means: torch.Tensor, k_means: torch.Tensor, tau: float, n_pre
 
 def sparse_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, lists: torch.Tensor,
                      counts: torch.Tensor, n_rows: int, scale: Optional[float] = None,
-                     out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """Attention of each query row over the KV blocks its block keeps."""
+                     out: Optional[torch.Tensor] = None, stream=None,
+                     n_prefix_blocks: int = 0) -> torch.Tensor:
+    """Attention of each query row over the KV blocks its block keeps.
+
+    ``n_prefix_blocks`` (the value given to ``block_select``) only orders the
+    work: the dense prefix query tiles are scheduled first."""
     H = q.shape[1]
     if out is None:
         out = torch.empty((q.shape[0], H, HEAD_DIM), dtype=torch.bfloat16, device=q.device)
@@ -301,7 +305,7 @@ def sparse_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, lists: t
     _check(lib().h3_sparse_attention(q.data_ptr(), strides[0], k.data_ptr(), strides[1],
                                      v.data_ptr(), strides[2], out.data_ptr(), strides[3],
                                      int(n_rows), H, HEAD_DIM, lists.data_ptr(), counts.data_ptr(),
-                                     float(scale), _stream(stream)))
+                                     int(n_prefix_blocks), float(scale), _stream(stream)))
     return out
 
 
@@ -309,8 +313,9 @@ def sol_attention(q, k, v, n_rows: int, tau: float, n_prefix_rows: int,
                   scale: Optional[float] = None, out=None, stream=None):
     """The three block-sparse stages in a row; returns (out, lists, counts)."""
     qm, km = block_means_qk(q, k, n_rows, stream)
-    lists, counts = block_select(qm, km, tau, -(-n_prefix_rows // BLOCK), scale, stream=stream)
-    out = sparse_attention(q, k, v, lists, counts, n_rows, scale, out, stream)
+    n_pre = -(-n_prefix_rows // BLOCK)
+    lists, counts = block_select(qm, km, tau, n_pre, scale, stream=stream)
+    out = sparse_attention(q, k, v, lists, counts, n_rows, scale, out, stream, n_prefix_blocks=n_pre)
     return out, lists, counts
 
 

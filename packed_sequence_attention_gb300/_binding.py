@@ -44,7 +44,7 @@ SIGNATURES = {
                                 c_void_p, c_void_p, c_void_p, c_void_p]),
     "h3_sparse_attention": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_int64,
                                     c_void_p, c_int64, c_int64, c_int, c_int, c_void_p, c_void_p,
-                                    c_float, c_void_p]),
+                                    c_int, c_float, c_void_p]),
     "h3_wire_record_bytes": (c_int, [c_int, c_int]),
     "h3_pack_qkv": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_int64, c_int64,
                             c_int, c_int, c_int, c_void_p, c_void_p]),

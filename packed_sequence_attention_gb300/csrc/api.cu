@@ -427,13 +427,18 @@ int h3_block_select(const float* q_means, const float* k_means, int n_q_blocks, 
 int h3_sparse_attention(const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,
                         const void* v, int64_t v_row_stride, void* out, int64_t out_row_stride,
                         int64_t n_rows, int n_heads, int head_dim, const int32_t* lists,
-                        const int32_t* counts, float scale, h3_stream_t stream) {
+                        const int32_t* counts, int n_prefix_blocks, float scale,
+                        h3_stream_t stream) {
   if (n_rows < 1 || n_rows > int64_t(h3::kMaxSparseBlocks) * 128)
     return fail(H3_ERR_ARG, "n_rows must be in [1, %d] (got %lld)", h3::kMaxSparseBlocks * 128,
                 (long long)n_rows);
   if (n_heads < 1) return fail(H3_ERR_ARG, "n_heads must be >= 1 (got %d)", n_heads);
   if (head_dim != h3::kHeadDim) return fail(H3_ERR_SHAPE, "head_dim must be 128 (got %d)", head_dim);
   if (!std::isfinite(scale) || !(scale > 0.0f)) return fail(H3_ERR_ARG, "scale must be finite and > 0");
+  const int64_t n_b = (n_rows + 127) / 128;
+  if (n_prefix_blocks < 0 || n_prefix_blocks > n_b)
+    return fail(H3_ERR_ARG, "n_prefix_blocks must be in [0, %lld] (got %d)", (long long)n_b,
+                n_prefix_blocks);
   const int64_t width = static_cast<int64_t>(n_heads) * h3::kHeadDim;
   if (q_row_stride < width || k_row_stride < width || v_row_stride < width || out_row_stride < width)
     return fail(H3_ERR_SHAPE, "row strides must be >= n_heads*128 = %lld", (long long)width);
@@ -464,6 +469,7 @@ int h3_sparse_attention(const void* q, int64_t q_row_stride, const void* k, int6
   a.lists = lists;
   a.counts = counts;
   a.scale = scale;
+  a.n_prefix_blocks = n_prefix_blocks;
   std::string err;
   st = h3::launch_sparse_attention(a, reinterpret_cast<cudaStream_t>(stream), err);
   if (st != H3_OK) return fail(st, "%s", err.c_str());

@@ -75,9 +75,10 @@ enum {
 };
 constexpr uint32_t kOffTmemSlot = kOffBar + NUM_BARS * 8;
 constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
+constexpr uint32_t kOffQIssued = kOffAbort + 4;  // 1 once the Q copy is in flight
 // Block-sparse mode only: int [4] = union length, steps both tiles keep,
 // alternating pairs, the tile of the remaining steps; then the lists.
-constexpr uint32_t kOffList = kOffAbort + 4;
+constexpr uint32_t kOffList = kOffQIssued + 12;
 constexpr uint32_t kListWords = kMaxSparseBlocks / 32;
 constexpr uint32_t kOffListBits = kOffList + 16;                   // [2][kListWords] u32
 constexpr uint32_t kOffListTiles = kOffListBits + 2 * kListWords * 4;  // [kMaxSparseBlocks] u16
@@ -123,6 +124,7 @@ struct __align__(128) AttnParams {
   const int32_t* sp_counts;  // [H, nqb]
   int32_t sp_nqb, sp_nkb;
   int32_t sp_tail;           // valid rows of the last KV block
+  int32_t sp_heavy;          // leading query-tile pairs of every head scheduled first
 };
 
 struct WaitCtx {
@@ -255,8 +257,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   while (si + 1 < p.n_seg && static_cast<int>(blockIdx.x) >= p.seg[si + 1].cta0) ++si;
   const Seg sg = p.seg[si];
   const int local = static_cast<int>(blockIdx.x) - sg.cta0;
-  const int head = local / sg.n_pairs;
-  const int qrow0 = (local - head * sg.n_pairs) * (2 * kBM);  // segment-relative
+  int head, pair;
+  if (kSparse && local < p.sp_heavy * p.n_heads) {
+    // Block-sparse: the tiles of the dense prefix queries (every KV block
+    // kept) are several times longer than the rest; they go first, head by
+    // head, so that none of them starts in the last waves.
+    head = local / p.sp_heavy;
+    pair = local - head * p.sp_heavy;
+  } else {
+    const int heavy = kSparse ? p.sp_heavy : 0;
+    const int rest = sg.n_pairs - heavy;
+    const int l2 = local - heavy * p.n_heads;
+    head = l2 / rest;
+    pair = heavy + (l2 - head * rest);
+  }
+  const int qrow0 = pair * (2 * kBM);  // segment-relative
   const int n_tiles = (qrow0 + kBM < sg.nq) ? 2 : 1;
   // KV tiles: those of the first view, then those of the second; the online
   // softmax does not depend on the order in which keys are visited.
@@ -264,6 +279,40 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   int n_kv = n_kv1 + (sg.nkv2 + kBN - 1) / kBN;
   const uint16_t* list_tiles = reinterpret_cast<const uint16_t*>(gbase + kOffListTiles);
   const uint8_t* list_sel = gbase + kOffListSel;
+  // Set-up by the producer's lane: barriers, then the Q tiles' load, so that
+  // Q lands while the other warps zero padded rows, build the block lists
+  // and allocate TMEM.  Nothing else touches a barrier before the block-wide
+  // barrier below.
+  volatile uint32_t* q_issued = reinterpret_cast<volatile uint32_t*>(gbase + kOffQIssued);
+  if (warp == 8 && lane == 0) {
+    *q_issued = 0u;
+    mbar_init(bar(BAR_Q), 1);
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(bar(BAR_KFULL + s), 1);
+      mbar_init(bar(BAR_VFULL + s), 1);
+      mbar_init(bar(BAR_KEMPTY + s), 1);
+      mbar_init(bar(BAR_VEMPTY + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(BAR_SFULL + t), 1);
+      mbar_init(bar(BAR_PFULL + t), 4);  // one arrive per softmax warp
+      mbar_init(bar(BAR_OFINAL + t), 1);
+    }
+    mbar_init(bar(BAR_DRAIN), 1);
+    fence_mbar_init();
+    *abort_flag =
+        (*reinterpret_cast<volatile uint32_t*>(&g_abort_epoch) == p.epoch) ? 1u : 0u;
+    if (*abort_flag == 0u) {
+      const CUtensorMap* tq = &p.tm_q[si];
+      prefetch_tmap(tq);
+      mbar_arrive_expect_tx(bar(BAR_Q), n_tiles * kTileBytes);
+      for (int t = 0; t < n_tiles; ++t)
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(sbase + kOffQ + t * kTileBytes + h * kHalfBytes, tq, bar(BAR_Q), h * 64,
+                      head, qrow0 + t * kBM);
+      *q_issued = 1u;
+    }
+  }
   if (kSparse) {
     // Ordered union of the two query tiles' kept KV blocks (warp 2).
     if (warp == 2) {
@@ -354,25 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
   }
 
-  // ---- set-up: barriers (thread 0), TMEM (warp 9)
-  if (threadIdx.x == 0) {
-    mbar_init(bar(BAR_Q), 1);
-    for (int s = 0; s < kNS; ++s) {
-      mbar_init(bar(BAR_KFULL + s), 1);
-      mbar_init(bar(BAR_VFULL + s), 1);
-      mbar_init(bar(BAR_KEMPTY + s), 1);
-      mbar_init(bar(BAR_VEMPTY + s), 1);
-    }
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(bar(BAR_SFULL + t), 1);
-      mbar_init(bar(BAR_PFULL + t), 4);  // one arrive per softmax warp
-      mbar_init(bar(BAR_OFINAL + t), 1);
-    }
-    mbar_init(bar(BAR_DRAIN), 1);
-    fence_mbar_init();
-    *abort_flag =
-        (*reinterpret_cast<volatile uint32_t*>(&g_abort_epoch) == p.epoch) ? 1u : 0u;
-  }
+  // ---- set-up: TMEM (warp 9)
   if (warp == 9) {
     tmem_alloc(sbase + kOffTmemSlot, kTmemCols);
     tmem_relinquish();
@@ -388,23 +419,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   if (warp == 8) {
     // ================================================= TMA producer
     if (lane == 0 && *abort_flag == 0u && !no_keys) {
-      const CUtensorMap* tq = &p.tm_q[si];
       const CUtensorMap* tk1 = &p.tm_k[si];
       const CUtensorMap* tv1 = &p.tm_v[si];
       const CUtensorMap* tk2 = &p.tm_k2[si];
       const CUtensorMap* tv2 = &p.tm_v2[si];
-      prefetch_tmap(tq);
       prefetch_tmap(tk1);
       prefetch_tmap(tv1);
       if (sg.nkv2 > 0) {
         prefetch_tmap(tk2);
         prefetch_tmap(tv2);
       }
-      mbar_arrive_expect_tx(bar(BAR_Q), n_tiles * kTileBytes);
-      for (int t = 0; t < n_tiles; ++t)
-        for (int h = 0; h < 2; ++h)
-          tma_load_3d(sbase + kOffQ + t * kTileBytes + h * kHalfBytes, tq, bar(BAR_Q), h * 64,
-                      head, qrow0 + t * kBM);
       int armed_k[kNS], armed_v[kNS];
       for (int s = 0; s < kNS; ++s) armed_k[s] = armed_v[s] = -1;
       bool ok = true;
@@ -438,6 +462,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           if (armed_v[s] >= 0) drain_wait(bar(BAR_VFULL + s), armed_v[s] & 1);
         }
       }
+    } else if (lane == 0 && *q_issued != 0u) {
+      drain_wait(bar(BAR_Q), 0);  // no K/V to load: let the Q copy land before the CTA exits
     }
     __syncwarp();  // lanes 1-31 wait here for lane 0
   } else if (warp == 9) {
@@ -928,6 +954,7 @@ struct SparseLists {
   const int32_t* lists;
   const int32_t* counts;
   int nqb, nkb, tail;
+  int heavy_pairs;  // leading query-tile pairs scheduled first
 };
 
 int launch_items(const Buffers& b, std::vector<Item>& items,
@@ -999,6 +1026,7 @@ int launch_items(const Buffers& b, std::vector<Item>& items,
     P.sp_nqb = sparse->nqb;
     P.sp_nkb = sparse->nkb;
     P.sp_tail = sparse->tail;
+    P.sp_heavy = sparse->heavy_pairs;
   }
   int64_t grid = ctas;
   if (grid == 0) {
@@ -1072,7 +1100,10 @@ int launch_sparse_attention(const SparseAttnArgs& a, cudaStream_t stream, std::s
   const Buffers bufs{a.q, a.k, a.v, nullptr, nullptr, a.out,
                      a.q_stride, a.k_stride, a.v_stride, 0, 0, a.out_stride};
   const int nb = static_cast<int>((a.n_rows + kBN - 1) / kBN);
-  const SparseLists sl{a.lists, a.counts, nb, nb, static_cast<int>(a.n_rows - (nb - 1) * kBN)};
+  const int n_pairs = (nb + 1) / 2;
+  const int heavy = std::min((a.n_prefix_blocks + 1) / 2, n_pairs);
+  const SparseLists sl{a.lists, a.counts, nb, nb, static_cast<int>(a.n_rows - (nb - 1) * kBN),
+                       heavy};
   return launch_items(bufs, items, zero, a.n_heads, a.scale, stream, err, &sl);
 }
 

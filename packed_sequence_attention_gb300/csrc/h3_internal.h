@@ -93,6 +93,7 @@ struct SparseAttnArgs {
   const int32_t* lists;   // device [H, nb, nb]
   const int32_t* counts;  // device [H, nb]
   float scale;
+  int n_prefix_blocks;    // scheduling hint: dense prefix query blocks
 };
 int launch_sparse_attention(const SparseAttnArgs& a, cudaStream_t stream, std::string& err);
 

@@ -187,13 +187,15 @@ def test_block_select_rejects_on_host(lib, args, code):
 @pytest.mark.parametrize("args,code", [
     (dict(n=0), ARG), (dict(D=256), SHAPE), (dict(lists=None), ARG), (dict(q=A + 2), ALIGN),
     (dict(os_=100), SHAPE), (dict(scale=-1.0), ARG), (dict(counts=A + 1), ALIGN),
+    (dict(npre=-1), ARG), (dict(npre=9), ARG),             # 1,000 rows: 8 blocks
 ])
 def test_sparse_attention_rejects_on_host(lib, args, code):
-    a = dict(q=A, k=A, v=A, o=A, os_=5376, n=1000, H=42, D=128, lists=A, counts=A, scale=0.1)
+    a = dict(q=A, k=A, v=A, o=A, os_=5376, n=1000, H=42, D=128, lists=A, counts=A, npre=0,
+             scale=0.1)
     a.update(args)
     assert lib.h3_sparse_attention(a["q"], 5376, a["k"], 5376, a["v"], 5376, a["o"], a["os_"],
-                                   a["n"], a["H"], a["D"], a["lists"], a["counts"], a["scale"],
-                                   None) == code
+                                   a["n"], a["H"], a["D"], a["lists"], a["counts"], a["npre"],
+                                   a["scale"], None) == code
 
 
 def test_wire_record_sizes_on_host(lib):

@@ -123,7 +123,7 @@ def test_block_sparse_stages():
     _, out, ok = guarded_rows(rows, H, extra_rows=2)
     assert lib.h3_sparse_attention(q.data_ptr(), H * 128, k.data_ptr(), H * 128, v.data_ptr(),
                                    H * 128, out.data_ptr(), out.stride(0), rows, H, 128, gl.ptr(),
-                                   gc.ptr(), SCALE, None) == 0
+                                   gc.ptr(), 1, SCALE, None) == 0
     torch.cuda.synchronize()
     assert all(g.margins_intact() for g in (*gm, *gqk, gl, gc, gs)) and ok()
 

@@ -135,8 +135,11 @@ def test_block_stages_and_sparse_attention(H, rows, tau, prefix):
     assert torch.equal(qm.view(torch.int32), qm2.view(torch.int32))
     assert torch.equal(km.view(torch.int32), km2.view(torch.int32))
     lists, counts, scores = h3.block_select(qm, km, tau, n_pre, SCALE, with_scores=True)
-    out = h3.sparse_attention(q, k, v, lists, counts, rows, SCALE)
+    out = h3.sparse_attention(q, k, v, lists, counts, rows, SCALE, n_prefix_blocks=n_pre)
+    # the prefix hint only reorders the work: the output is the same bits
+    out0 = h3.sparse_attention(q, k, v, lists, counts, rows, SCALE, n_prefix_blocks=0)
     torch.cuda.synchronize()
+    assert torch.equal(out[:rows].view(torch.int16), out0[:rows].view(torch.int16))
     qmr, kmr = O.block_means(O.widen(q), rows, B), O.block_means(O.widen(k), rows, B)
     assert np.abs(qm.double().cpu().numpy() - qmr).max() <= 1e-5
     assert np.abs(km.double().cpu().numpy() - kmr).max() <= 1e-5
