@@ -763,9 +763,78 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           ++j;
         }
         // Alternating phase: step j belongs to tile (j - nb) & 1, whose next
-        // step is j + 2, or the first step of the last phase.
-        // Unrolled by two (tile 0, then tile 1), so that the tile is a
-        // constant in each step's code.
+        // step is j + 2, or the first step of the last phase.  Pairs of
+        // steps (tile 0 at j, tile 1 at j + 1) whose next steps stay in the
+        // phase run as straight-line code in which every barrier and
+        // descriptor is fixed (j advances by 2, so the ring stages do not
+        // change).  Each step also probes, without waiting, the P and V
+        // barriers of the step after it before its commits, so that the next
+        // step skips their round trip when they have completed.
+        if (ok && j + 3 < na_end) {
+          const uint32_t sa = static_cast<uint32_t>(j) & 1u, sb = sa ^ 1u;
+          const uint32_t pbar0 = bar(BAR_PFULL), pbar1 = bar(BAR_PFULL + 1);
+          const uint32_t vfa = bar(BAR_VFULL + sa), vfb = bar(BAR_VFULL + sb);
+          const uint32_t kfa = bar(BAR_KFULL + sa), kfb = bar(BAR_KFULL + sb);
+          const uint32_t vea = bar(BAR_VEMPTY + sa), veb = bar(BAR_VEMPTY + sb);
+          const uint32_t kea = bar(BAR_KEMPTY + sa), keb = bar(BAR_KEMPTY + sb);
+          const uint32_t sf0 = bar(BAR_SFULL), sf1 = bar(BAR_SFULL + 1);
+          const uint64_t vda = sa ? vb1 : vb0, vdb = sa ? vb0 : vb1;
+          const uint64_t kda = sa ? kb1 : kb0, kdb = sa ? kb0 : kb1;
+          bool p_known = false, v_known = false;  // probed complete by the previous step
+          for (; j + 3 < na_end && ok; j += 2) {
+            const uint32_t hj = static_cast<uint32_t>(j) >> 1;
+            // tile 0: P0 . V(j), then Q0 . K(j + 2)^T
+            {
+              const uint32_t pp = static_cast<uint32_t>(kept0) & 1u, vp = hj & 1u;
+              const uint32_t kp = (hj + 1u) & 1u;
+              const bool p_ok = p_known || mbar_try_wait(pbar0, pp);
+              const bool v_ok = v_known || mbar_try_wait(vfa, vp);
+              const bool k_ok = mbar_test_wait(kfa, kp);
+              bool r = p_ok || wait1(pbar0, pp, wctx, H3_STATUS_TIMEOUT_MMA);
+              r = r && (v_ok || wait1(vfa, vp, wctx, H3_STATUS_TIMEOUT_MMA));
+              if (!r) { ok = false; break; }
+              tc_fence_after();
+              pv_(dO0, dS0, vda, kept0 > 0 ? 1u : 0u);
+              mma_commit(vea);
+              if (!k_ok) {
+                if (!wait1(kfa, kp, wctx, H3_STATUS_TIMEOUT_MMA)) { ok = false; break; }
+                tc_fence_after();
+              }
+              qk_(dS0, qa0, kda);
+              p_known = mbar_test_wait(pbar1, static_cast<uint32_t>(kept1) & 1u);
+              v_known = mbar_test_wait(vfb, (static_cast<uint32_t>(j + 1) >> 1) & 1u);
+              mma_commit(sf0);
+              mma_commit(kea);
+              ++kept0;
+            }
+            // tile 1: P1 . V(j + 1), then Q1 . K(j + 3)^T
+            {
+              const uint32_t pp = static_cast<uint32_t>(kept1) & 1u;
+              const uint32_t vp = (static_cast<uint32_t>(j + 1) >> 1) & 1u;
+              const uint32_t kp = (static_cast<uint32_t>(j + 3) >> 1) & 1u;
+              const bool p_ok = p_known || mbar_try_wait(pbar1, pp);
+              const bool v_ok = v_known || mbar_try_wait(vfb, vp);
+              const bool k_ok = mbar_test_wait(kfb, kp);
+              bool r = p_ok || wait1(pbar1, pp, wctx, H3_STATUS_TIMEOUT_MMA);
+              r = r && (v_ok || wait1(vfb, vp, wctx, H3_STATUS_TIMEOUT_MMA));
+              if (!r) { ok = false; break; }
+              tc_fence_after();
+              pv_(dO1, dS1, vdb, kept1 > 0 ? 1u : 0u);
+              mma_commit(veb);
+              if (!k_ok) {
+                if (!wait1(kfb, kp, wctx, H3_STATUS_TIMEOUT_MMA)) { ok = false; break; }
+                tc_fence_after();
+              }
+              qk_(dS1, qa1, kdb);
+              p_known = mbar_test_wait(pbar0, static_cast<uint32_t>(kept0) & 1u);
+              v_known = mbar_test_wait(vfa, ((hj + 1u) & 1u));
+              mma_commit(sf1);
+              mma_commit(keb);
+              ++kept1;
+            }
+          }
+        }
+        // The phase's last pair hands each tile over to its next step.
         for (; j < na_end && ok; j += 2) {
           const int n0 = j + 2 < na_end ? j + 2 : ((rt == 0 && na_end < n_kv) ? na_end : n_kv);
           ok = step1(0, j, kept0, n0);
