@@ -212,8 +212,13 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_con
       sn[j] = v.y;
     }
     const uint32_t stage = sbase + s * stage_bytes;
+    // The slots of the last, partial pass (n_heads % 16 of them) move to
+    // other warps from one item to the next, so that every warp does the
+    // same work on average: a stage is released only when its slowest warp
+    // is done.
+    const int rslot = (slot + 4 * static_cast<int>(i & 3)) & (kSlots - 1);
     for (int u0 = 0; u0 < n_units; u0 += kSlots) {
-      const int u = u0 + slot;
+      const int u = u0 + rslot;
       const bool live = u < n_units;
       const int t = tsel;
       const int h = live ? u : 0;
