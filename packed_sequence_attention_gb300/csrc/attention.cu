@@ -322,14 +322,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const int nwords = (p.sp_nkb + 31) / 32;
       for (int w = lane; w < 2 * static_cast<int>(kListWords); w += 32) bits[w] = 0u;
       __syncwarp();
-      for (int t = 0; t < n_tiles; ++t) {
-        const int64_t row = static_cast<int64_t>(head) * p.sp_nqb + (qrow0 / kBM + t);
-        int cnt = p.sp_counts[row];
-        cnt = cnt < 0 ? 0 : (cnt > p.sp_nkb ? p.sp_nkb : cnt);  // lists are not trusted
-        const int32_t* lst = p.sp_lists + row * p.sp_nkb;
-        for (int i = lane; i < cnt; i += 32) {
-          const int b = lst[i];
-          if (b >= 0 && b < p.sp_nkb) atomicOr(&bits[t * kListWords + (b >> 5)], 1u << (b & 31));
+      // Both tiles' counts, then their entries in batches of 8 per lane and
+      // tile, every load of a batch in flight before the first is used: a
+      // handful of global round trips before the first K/V copy can start,
+      // instead of one per 32 entries.
+      const int64_t row0 = static_cast<int64_t>(head) * p.sp_nqb + qrow0 / kBM;
+      const int c0 = __ldg(p.sp_counts + row0);
+      const int c1 = n_tiles == 2 ? __ldg(p.sp_counts + row0 + 1) : 0;
+      const int cnt0 = c0 < 0 ? 0 : (c0 > p.sp_nkb ? p.sp_nkb : c0);  // lists are not trusted
+      const int cnt1 = c1 < 0 ? 0 : (c1 > p.sp_nkb ? p.sp_nkb : c1);
+      const int32_t* lst0 = p.sp_lists + row0 * p.sp_nkb;
+      const int32_t* lst1 = lst0 + p.sp_nkb;
+      const int cmax = cnt0 > cnt1 ? cnt0 : cnt1;
+      for (int base = 0; base < cmax; base += 8 * 32) {
+        int e0[8], e1[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = base + u * 32 + lane;
+          e0[u] = i < cnt0 ? __ldg(lst0 + i) : -1;
+          e1[u] = i < cnt1 ? __ldg(lst1 + i) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (e0[u] >= 0 && e0[u] < p.sp_nkb) atomicOr(&bits[e0[u] >> 5], 1u << (e0[u] & 31));
+          if (e1[u] >= 0 && e1[u] < p.sp_nkb)
+            atomicOr(&bits[kListWords + (e1[u] >> 5)], 1u << (e1[u] & 31));
         }
       }
       __syncwarp();
