@@ -327,14 +327,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       // handful of global round trips before the first K/V copy can start,
       // instead of one per 32 entries.
       const int64_t row0 = static_cast<int64_t>(head) * p.sp_nqb + qrow0 / kBM;
+      const int32_t* lst0 = p.sp_lists + row0 * p.sp_nkb;
+      const int32_t* lst1 = lst0 + p.sp_nkb;
+      // The first batch is read before the counts are known (every row holds
+      // n_kv_blocks entries), so that it shares their round trip.
+      int f0[8], f1[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = u * 32 + lane;
+        f0[u] = i < p.sp_nkb ? __ldg(lst0 + i) : -1;
+        f1[u] = (n_tiles == 2 && i < p.sp_nkb) ? __ldg(lst1 + i) : -1;
+      }
       const int c0 = __ldg(p.sp_counts + row0);
       const int c1 = n_tiles == 2 ? __ldg(p.sp_counts + row0 + 1) : 0;
       const int cnt0 = c0 < 0 ? 0 : (c0 > p.sp_nkb ? p.sp_nkb : c0);  // lists are not trusted
       const int cnt1 = c1 < 0 ? 0 : (c1 > p.sp_nkb ? p.sp_nkb : c1);
-      const int32_t* lst0 = p.sp_lists + row0 * p.sp_nkb;
-      const int32_t* lst1 = lst0 + p.sp_nkb;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = u * 32 + lane;
+        if (i < cnt0 && f0[u] >= 0 && f0[u] < p.sp_nkb)
+          atomicOr(&bits[f0[u] >> 5], 1u << (f0[u] & 31));
+        if (i < cnt1 && f1[u] >= 0 && f1[u] < p.sp_nkb)
+          atomicOr(&bits[kListWords + (f1[u] >> 5)], 1u << (f1[u] & 31));
+      }
       const int cmax = cnt0 > cnt1 ? cnt0 : cnt1;
-      for (int base = 0; base < cmax; base += 8 * 32) {
+      for (int base = 8 * 32; base < cmax; base += 8 * 32) {
         int e0[8], e1[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -861,15 +878,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           ok = step1(1, j + 1, kept1, n1);
           ++kept1;
         }
+        // The other tile has no step left: its output can be written while
+        // tile rt runs the last phase.
+        const int other_kept = rt ? kept0 : kept1;
+        if (ok && other_kept > 0) mma_commit(bar(BAR_OFINAL + (1 - rt)));
         // Last phase: one tile, step after step.
         for (; j < n_kv && ok; ++j) {
           ok = step1(rt, j, rt ? kept1 : kept0, j + 1);
           if (rt) ++kept1; else ++kept0;
         }
-        if (ok) {
-          if (kept0 > 0) mma_commit(bar(BAR_OFINAL));
-          if (kept1 > 0) mma_commit(bar(BAR_OFINAL + 1));
-        }
+        if (ok && (rt ? kept1 : kept0) > 0) mma_commit(bar(BAR_OFINAL + rt));
       }
       // Every MMA issued above completes before TMEM is released.
       mma_commit(bar(BAR_DRAIN));
