@@ -138,8 +138,20 @@ def whole_job_value(units_per_rank, ms_per_step, world):
 
 
 # -------------------------------------------------------------- the GPU arm
+def prologue_launches(w):
+    """One launch covers every sequence's valid rows (none when no row is valid)."""
+    return int(w.self_attention and any(s.n_valid_q() for s in w.segments))
+
+
 def launches_per_step(w):
-    return (len([s for s in w.segments if s.n_valid_q() > 0]) if w.self_attention else 0) + 1
+    return prologue_launches(w) + 1
+
+
+def run_prologue(h3, g, w):
+    """The prologue on every sequence's valid rows, in one launch."""
+    if prologue_launches(w):
+        h3.qk_norm_rope_varlen(g["q"], g["k"], g["wq"], g["wk"], g["pos_thw"], g["cu_seqlens_q"],
+                               g["valid_len"], rot=ROT)
 
 
 def run_step(h3, g, w, ev=None):
@@ -147,12 +159,7 @@ def run_step(h3, g, w, ev=None):
     (four events), records prologue and attention boundaries."""
     if ev is not None:
         ev[0].record()
-    if w.self_attention:
-        for b, s in enumerate(w.segments):
-            if s.n_valid_q():
-                r0 = g["cu_seqlens_q"][b]
-                h3.qk_norm_rope(g["q"][r0:], g["k"][r0:], g["wq"], g["wk"], g["pos_thw"][r0:],
-                                n_rows=s.n_valid_q(), rot=ROT)
+    run_prologue(h3, g, w)
     if ev is not None:
         ev[1].record()
     h3.attention(g["q"], g["k"], g["v"], g["cu_seqlens_q"], g["cu_seqlens_kv"], g["valid_len"],
@@ -278,11 +285,7 @@ def bench_gpu(args):
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a0.record(stream)
         for _ in range(10):
-            for b, s in enumerate(w.segments):
-                if s.n_valid_q():
-                    r0 = g["cu_seqlens_q"][b]
-                    h3.qk_norm_rope(g["q"][r0:], g["k"][r0:], g["wq"], g["wk"],
-                                    g["pos_thw"][r0:], n_rows=s.n_valid_q(), rot=ROT)
+            run_prologue(h3, g, w)
         a1.record(stream)
         torch.cuda.synchronize()
         pro_alone_ms = a0.elapsed_time(a1) / 10
@@ -555,7 +558,7 @@ def config_sweep(h3, W, O, pk, names, min_timed_s=0.3):
             entry.update({"prologue_us": round(pro_ms * 1e3, 2), "prologue_gbs": round(gbs, 1),
                           "prologue_frac_hbm_measured": round(gbs / pk["hbm"], 4),
                           "prologue_frac_8tbs": round(gbs / 8000.0, 4),
-                          "prologue_launches": len([s for s in w.segments if s.n_valid_q()]),
+                          "prologue_launches": prologue_launches(w),
                           "prologue_bytes": w.prologue_bytes()})
         res[name] = entry
         del g, evs

@@ -95,6 +95,35 @@ int h3_qk_norm_rope(void* q, int64_t q_row_stride, void* k, int64_t k_row_stride
                     h3_stream_t stream);
 
 /*
+ * h3_qk_norm_rope_varlen -- the same prologue over the valid rows of several
+ * packed sequences, in one launch.
+ *
+ * The vLLM-Omni blog (section 3.1) denoises text, audio and video tokens as
+ * one packed sequence whose valid rows are followed by padding up to an
+ * aligned length.  Several such sequences may sit back to back in one buffer,
+ * in the layout h3_attention takes: sequence b is buffer rows
+ * [cu_seqlens[b], cu_seqlens[b + 1]), of which the first valid_len[b] are
+ * valid, and the prologue applies to those.  Each of those rows is processed
+ * exactly as by h3_qk_norm_rope (bitwise the same result); other rows are not
+ * read or written.  One persistent launch covers all sequences, so they pay
+ * one launch tail instead of one per sequence.
+ *
+ * q, k        device bf16 [cu_seqlens[n_seq], n_heads, 128], row strides in elements.
+ * pos_thw     device int32 [cu_seqlens[n_seq], 3], indexed by buffer row.
+ * cu_seqlens  HOST int32 [n_seq + 1], cu_seqlens[0] == 0, non-decreasing.
+ * valid_len   HOST int32 [n_seq], 0 <= valid_len[b] <= cu_seqlens[b + 1] - cu_seqlens[b];
+ *             NULL = every row of every sequence is valid.
+ * n_seq       1 .. H3_MAX_SEGMENTS; the valid rows sum to at most 2^30.
+ * All other arguments, alignment rules and errors as h3_qk_norm_rope.  The
+ * host arrays are read before the call returns.
+ */
+int h3_qk_norm_rope_varlen(void* q, int64_t q_row_stride, void* k, int64_t k_row_stride,
+                           const void* wq, const void* wk, const int32_t* pos_thw,
+                           const int32_t* cu_seqlens, const int32_t* valid_len, int n_seq,
+                           int n_heads, int head_dim, int rot_t, int rot_h, int rot_w,
+                           float theta, float eps, h3_stream_t stream);
+
+/*
  * h3_qk_norm_rope_lora -- the same fused prologue as a LoRA consumer.
  *
  * Follows "Precision-preserving LoRA fusion" (Sol-H3, section 3.5): the base

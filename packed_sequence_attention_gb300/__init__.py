@@ -5,7 +5,9 @@ Two operations, both hand-written CUDA behind the C ABI of libh3kern.so
 strides and the current stream:
 
 * ``qk_norm_rope`` -- fused Q/K RMSNorm + axial 3-D RoPE, in place
-  (Sol-H3, arXiv 2609.35110, section 3.5 "Kernel Fusion", operator group 2).
+  (Sol-H3, arXiv 2609.35110, section 3.5 "Kernel Fusion", operator group 2);
+  ``qk_norm_rope_varlen`` does the valid rows of several packed sequences in
+  one launch.
 * ``qk_norm_rope_lora`` -- the same as a LoRA consumer: base + delta is
   rounded to bf16 first (Sol-H3 section 3.5, precision-preserving LoRA fusion).
 * ``attention`` -- softmax(Q K^T * scale) V over packed sequences with a
@@ -34,7 +36,7 @@ import torch
 
 from . import _binding
 
-__all__ = ["H3Error", "qk_norm_rope", "qk_norm_rope_lora", "attention", "attention_groups",
+__all__ = ["H3Error", "qk_norm_rope", "qk_norm_rope_varlen", "qk_norm_rope_lora", "attention", "attention_groups",
            "block_means", "block_means_qk", "block_select", "sparse_attention", "sol_attention",
            "WIRE_BF16", "WIRE_INT8", "WIRE_FP8", "wire_record_bytes", "pack_qkv", "unpack_qkv",
            "pack_out", "merge_heads",
@@ -113,6 +115,34 @@ def qk_norm_rope(q: torch.Tensor, k: torch.Tensor, wq: torch.Tensor, wk: torch.T
                                  wk.data_ptr(), pos_thw.data_ptr(), int(n_rows), H, HEAD_DIM,
                                  int(rot[0]), int(rot[1]), int(rot[2]), float(theta),
                                  float(eps), _stream(stream)))
+
+
+def qk_norm_rope_varlen(q: torch.Tensor, k: torch.Tensor, wq: torch.Tensor, wk: torch.Tensor,
+                        pos_thw: torch.Tensor, cu_seqlens: Sequence[int],
+                        valid_len: Optional[Sequence[int]] = None, rot=(32, 48, 48),
+                        theta: float = 10000.0, eps: float = 1e-6, stream=None) -> None:
+    """In place, in one launch: ``qk_norm_rope`` on the first ``valid_len[b]``
+    rows of each packed sequence b = rows [cu_seqlens[b], cu_seqlens[b+1]).
+
+    ``cu_seqlens`` and ``valid_len`` are host sequences of ints; ``pos_thw``
+    is indexed by buffer row.  Other rows are not touched."""
+    qs, ks = _row_stride(q, "q"), _row_stride(k, "k")
+    H = q.shape[1]
+    _heads(k, "k", H)
+    n_seq = len(cu_seqlens) - 1
+    if valid_len is not None and len(valid_len) != n_seq:
+        raise ValueError("cu_seqlens and valid_len disagree on n_seq")
+    if n_seq >= 1 and cu_seqlens[-1] > min(q.shape[0], k.shape[0], pos_thw.shape[0]):
+        raise ValueError("cu_seqlens exceed the tensors")
+    _prologue_small_inputs(wq, wk, pos_thw, H)
+    cu = _i32_array(cu_seqlens)
+    vl = _i32_array(valid_len) if valid_len is not None else None
+    _check(lib().h3_qk_norm_rope_varlen(q.data_ptr(), qs, k.data_ptr(), ks, wq.data_ptr(),
+                                        wk.data_ptr(), pos_thw.data_ptr(),
+                                        ctypes.cast(cu, _binding.c_i32p),
+                                        ctypes.cast(vl, _binding.c_i32p) if vl is not None
+                                        else None, n_seq, H, HEAD_DIM, int(rot[0]), int(rot[1]),
+                                        int(rot[2]), float(theta), float(eps), _stream(stream)))
 
 
 def qk_norm_rope_lora(q: torch.Tensor, q_delta: torch.Tensor, k: torch.Tensor,
@@ -397,13 +427,10 @@ def attention_block(q, k, v, wq, wk, pos_thw, cu_seqlens, valid_len,
 
 
 def _block_prologue(q, k, wq, wk, pos_thw, cu_seqlens, valid_len, rot, theta, eps, stream):
-    """The norm + RoPE of ``attention_block``: each packed sequence's valid rows."""
-    for b in range(len(cu_seqlens) - 1):
-        r0 = cu_seqlens[b]
-        n = valid_len[b] if valid_len is not None else cu_seqlens[b + 1] - r0
-        if n:
-            qk_norm_rope(q[r0:], k[r0:], wq, wk, pos_thw[r0:], n_rows=n, rot=rot,
-                         theta=theta, eps=eps, stream=stream)
+    """The norm + RoPE of ``attention_block``: every packed sequence's valid
+    rows, in one launch."""
+    qk_norm_rope_varlen(q, k, wq, wk, pos_thw, cu_seqlens, valid_len, rot=rot, theta=theta,
+                        eps=eps, stream=stream)
 
 
 def copy_2d(dst: torch.Tensor, src: torch.Tensor, stream=None) -> None:

@@ -27,6 +27,9 @@ SIGNATURES = {
     "h3_qk_norm_rope": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_void_p,
                                 c_void_p, c_int64, c_int, c_int, c_int, c_int, c_int,
                                 c_float, c_float, c_void_p]),
+    "h3_qk_norm_rope_varlen": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_void_p,
+                                       c_void_p, c_i32p, c_i32p, c_int, c_int, c_int, c_int, c_int,
+                                       c_int, c_float, c_float, c_void_p]),
     "h3_qk_norm_rope_lora": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_int64,
                                      c_void_p, c_int64, c_void_p, c_void_p, c_void_p, c_int64,
                                      c_int, c_int, c_int, c_int, c_int, c_float, c_float,

@@ -98,13 +98,17 @@ const char* h3_last_error(void) { return t_last_error.c_str(); }
 
 namespace {
 
-// Shared checks and launch of the plain and LoRA-fused prologue.
+// Shared checks and launch of the plain, packed-sequence and LoRA-fused
+// prologue.  The rows are n_seg segments [seg_row0[b], seg_row0[b] + seg_rows[b])
+// of the buffers (already checked: non-negative, in order, not overlapping).
 int norm_rope_entry(void* q, int64_t q_row_stride, void* k, int64_t k_row_stride,
                     const void* dq, int64_t dq_row_stride, const void* dk, int64_t dk_row_stride,
                     bool lora, const void* wq, const void* wk, const int32_t* pos_thw,
-                    int64_t n_rows, int n_heads, int head_dim, int rot_t, int rot_h, int rot_w,
-                    float theta, float eps, h3_stream_t stream) {
-  if (n_rows < 0) return fail(H3_ERR_ARG, "n_rows must be >= 0 (got %lld)", (long long)n_rows);
+                    const int64_t* seg_row0, const int64_t* seg_rows, int n_seg, int n_heads,
+                    int head_dim, int rot_t, int rot_h, int rot_w, float theta, float eps,
+                    h3_stream_t stream) {
+  int64_t n_rows = 0;
+  for (int b = 0; b < n_seg; ++b) n_rows += seg_rows[b];
   if (n_heads < 1) return fail(H3_ERR_ARG, "n_heads must be >= 1 (got %d)", n_heads);
   if (head_dim != h3::kHeadDim) return fail(H3_ERR_SHAPE, "head_dim must be 128 (got %d)", head_dim);
   if (n_heads > h3::prologue_max_heads(lora))
@@ -139,7 +143,8 @@ int norm_rope_entry(void* q, int64_t q_row_stride, void* k, int64_t k_row_stride
       (lora && ((dq_row_stride * 2) % 16 != 0 || (dk_row_stride * 2) % 16 != 0)))
     return fail(H3_ERR_ALIGN, "row strides must be multiples of 8 elements (16 bytes)");
   if (n_rows > (int64_t(1) << 30))
-    return fail(H3_ERR_SHAPE, "n_rows too large for one launch");
+    return fail(H3_ERR_SHAPE, "%lld rows are too many for one launch (at most 2^30)",
+                (long long)n_rows);
   int st = check_device();
   if (st != H3_OK) return st;
   st = check_device_memory({{q, "q"}, {k, "k"}, {wq, "wq"}, {wk, "wk"}, {pos_thw, "pos_thw"},
@@ -153,7 +158,9 @@ int norm_rope_entry(void* q, int64_t q_row_stride, void* k, int64_t k_row_stride
   a.wq = static_cast<const __nv_bfloat16*>(wq);
   a.wk = static_cast<const __nv_bfloat16*>(wk);
   a.pos = pos_thw;
-  a.n_rows = n_rows;
+  a.seg_row0 = seg_row0;
+  a.seg_rows = seg_rows;
+  a.n_seg = n_seg;
   a.n_heads = n_heads;
   a.rot[0] = rot_t;
   a.rot[1] = rot_h;
@@ -179,9 +186,35 @@ int h3_qk_norm_rope(void* q, int64_t q_row_stride, void* k, int64_t k_row_stride
                     const void* wk, const int32_t* pos_thw, int64_t n_rows, int n_heads,
                     int head_dim, int rot_t, int rot_h, int rot_w, float theta, float eps,
                     h3_stream_t stream) {
+  if (n_rows < 0) return fail(H3_ERR_ARG, "n_rows must be >= 0 (got %lld)", (long long)n_rows);
+  const int64_t row0 = 0;
   return norm_rope_entry(q, q_row_stride, k, k_row_stride, nullptr, 0, nullptr, 0, false, wq, wk,
-                         pos_thw, n_rows, n_heads, head_dim, rot_t, rot_h, rot_w, theta, eps,
-                         stream);
+                         pos_thw, &row0, &n_rows, 1, n_heads, head_dim, rot_t, rot_h, rot_w,
+                         theta, eps, stream);
+}
+
+int h3_qk_norm_rope_varlen(void* q, int64_t q_row_stride, void* k, int64_t k_row_stride,
+                           const void* wq, const void* wk, const int32_t* pos_thw,
+                           const int32_t* cu_seqlens, const int32_t* valid_len, int n_seq,
+                           int n_heads, int head_dim, int rot_t, int rot_h, int rot_w,
+                           float theta, float eps, h3_stream_t stream) {
+  if (n_seq < 1 || n_seq > H3_MAX_SEGMENTS)
+    return fail(H3_ERR_ARG, "n_seq must be in [1, %d] (got %d)", H3_MAX_SEGMENTS, n_seq);
+  if (!cu_seqlens) return fail(H3_ERR_ARG, "null cu_seqlens");
+  if (cu_seqlens[0] != 0) return fail(H3_ERR_ARG, "cu_seqlens must start at 0");
+  int64_t row0[H3_MAX_SEGMENTS], rows[H3_MAX_SEGMENTS];
+  for (int b = 0; b < n_seq; ++b) {
+    if (cu_seqlens[b + 1] < cu_seqlens[b])
+      return fail(H3_ERR_ARG, "cu_seqlens must be non-decreasing (segment %d)", b);
+    const int32_t len = cu_seqlens[b + 1] - cu_seqlens[b];
+    if (valid_len && (valid_len[b] < 0 || valid_len[b] > len))
+      return fail(H3_ERR_ARG, "valid_len[%d] = %d outside [0, %d]", b, valid_len[b], len);
+    row0[b] = cu_seqlens[b];
+    rows[b] = valid_len ? valid_len[b] : len;
+  }
+  return norm_rope_entry(q, q_row_stride, k, k_row_stride, nullptr, 0, nullptr, 0, false, wq, wk,
+                         pos_thw, row0, rows, n_seq, n_heads, head_dim, rot_t, rot_h, rot_w,
+                         theta, eps, stream);
 }
 
 int h3_qk_norm_rope_lora(void* q, int64_t q_row_stride, const void* q_delta,
@@ -190,9 +223,11 @@ int h3_qk_norm_rope_lora(void* q, int64_t q_row_stride, const void* q_delta,
                          const void* wk, const int32_t* pos_thw, int64_t n_rows, int n_heads,
                          int head_dim, int rot_t, int rot_h, int rot_w, float theta, float eps,
                          h3_stream_t stream) {
+  if (n_rows < 0) return fail(H3_ERR_ARG, "n_rows must be >= 0 (got %lld)", (long long)n_rows);
+  const int64_t row0 = 0;
   return norm_rope_entry(q, q_row_stride, k, k_row_stride, q_delta, q_delta_row_stride, k_delta,
-                         k_delta_row_stride, true, wq, wk, pos_thw, n_rows, n_heads, head_dim,
-                         rot_t, rot_h, rot_w, theta, eps, stream);
+                         k_delta_row_stride, true, wq, wk, pos_thw, &row0, &n_rows, 1, n_heads,
+                         head_dim, rot_t, rot_h, rot_w, theta, eps, stream);
 }
 
 int h3_attention(const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,

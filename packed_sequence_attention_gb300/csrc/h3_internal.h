@@ -17,14 +17,20 @@ constexpr int kHeadDim = 128;
 constexpr int kMaxSparseBlocks = 2048;
 
 // ---------------------------------------------------------------- prologue
+// Packed sequences one prologue launch covers at most.
+constexpr int kPrologueMaxSegments = H3_MAX_SEGMENTS;
+
 struct NormRopeArgs {
   __nv_bfloat16* q;
   __nv_bfloat16* k;
   int64_t q_stride, k_stride;  // elements
   const __nv_bfloat16* wq;
   const __nv_bfloat16* wk;
-  const int32_t* pos;
-  int64_t n_rows;
+  const int32_t* pos;          // indexed by buffer row
+  // The rows to process: segment b is buffer rows [seg_row0[b], seg_row0[b] + seg_rows[b]).
+  const int64_t* seg_row0;     // host [n_seg]
+  const int64_t* seg_rows;     // host [n_seg]
+  int n_seg;
   int n_heads;
   int rot[3];
   float theta, eps;

@@ -6,8 +6,16 @@
 // RoPE.  The point of the fusion is to read each wide activation once and
 // write it once, so the kernel is built around keeping HBM busy:
 //
-// * Persistent CTAs walk items g = blockIdx.x + i * gridDim.x; item g is row
-//   g / 2 of Q (g even) or of K (g odd): n_heads * 256 contiguous bytes.
+// * Persistent CTAs walk items g = blockIdx.x + i * gridDim.x; item g is
+//   valid row g / 2 of Q (g even) or of K (g odd): n_heads * 256 contiguous
+//   bytes.  Valid rows are numbered across the packed sequences of the
+//   launch (the valid rows of each, in order), so several sequences share one
+//   persistent grid and pay one tail.  The streaming warp holds the sequence
+//   table (at most 16 entries) in its lanes' registers, maps each item's valid
+//   row to its buffer row with a ballot and two shuffles, and hands that row
+//   to the compute warps in the item's stage.  (Reading the table from the
+//   kernel parameters with a run-time index on every item cost 4 % on the
+//   58,758-row workload.)
 // * Warp roles.  One streaming warp copies items into a 3-stage shared-memory
 //   ring with 1-D bulk async copies (cp.async.bulk, completion on a "full"
 //   mbarrier) and fills each stage's (cos, sin) table for the item's
@@ -57,10 +65,13 @@ struct NormRopeParams {
   const __nv_bfloat16* w[2];
   const int32_t* pos;
   uint32_t* status;
-  int64_t n_rows;
+  int64_t n_rows;  // valid rows over all segments
   int n_heads;
   int n_stages;
   float eps;
+  int n_seg;
+  int32_t seg_cum[kPrologueMaxSegments + 1];  // valid rows before segment b; [n_seg] = n_rows
+  int64_t seg_row0[kPrologueMaxSegments];     // buffer row of segment b's first valid row
   float inv_freq[64];  // per channel pair p = (2p, 2p+1): theta^(-2j/d) of its section
   int32_t axis[64];    // 0 = t, 1 = h, 2 = w, -1 = not rotated
 };
@@ -139,10 +150,14 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_con
   float2* tab = reinterpret_cast<float2*>(smem + NST * stage_bytes);  // [NST][64] (cos, sin)
   const uint32_t full_bar = sbase + NST * stage_bytes + NST * 64 * 8;  // mbarriers [NST]
   const uint32_t empty_bar = full_bar + 8 * kMaxStages;                // mbarriers [NST]
+  // Buffer row of the item in each stage, written by the streaming warp
+  // before it arrives on the stage's full barrier.
+  int64_t* stage_row = reinterpret_cast<int64_t*>(smem + NST * stage_bytes + NST * 64 * 8 +
+                                                  16 * kMaxStages);
 
   const int64_t first = blockIdx.x;
   const int64_t step = gridDim.x;
-  const int64_t n_items = 2 * p.n_rows;  // item g: row g >> 1, tensor g & 1
+  const int64_t n_items = 2 * p.n_rows;  // item g: valid row g >> 1, tensor g & 1
   const int64_t n_mine = first < n_items ? (n_items - 1 - first) / step + 1 : 0;
 
   if (tid == 0) {
@@ -167,11 +182,24 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_con
     // ------------------------------------------------------------ streaming
     const int ax0 = p.axis[lane], ax1 = p.axis[lane + 32];
     const float f0 = p.inv_freq[lane], f1 = p.inv_freq[lane + 32];
-    auto pos_of = [&](int64_t i, int ax) -> int32_t {
-      if (ax < 0 || i >= n_mine) return 0;
-      return __ldg(p.pos + ((first + i * step) >> 1) * 3 + ax);
+    // The segment table in registers: lane b < n_seg holds segment b's
+    // cumulative valid count and first buffer row.  The segment of valid row
+    // r is the last one whose count is <= r (empty segments share their
+    // count with the next one, which comes later): one ballot, two shuffles.
+    const int32_t cum_l = lane < p.n_seg ? p.seg_cum[lane] : INT32_MAX;
+    const int64_t row0_l = lane < p.n_seg ? p.seg_row0[lane] : 0;
+    auto row_of = [&](int64_t i) -> int64_t {
+      const int64_t r = (first + i * step) >> 1;
+      const int b = __popc(__ballot_sync(0xffffffffu, cum_l <= r)) - 1;
+      return __shfl_sync(0xffffffffu, row0_l, b) + (r - __shfl_sync(0xffffffffu, cum_l, b));
     };
-    int32_t pn0 = pos_of(0, ax0), pn1 = pos_of(0, ax1);
+    // Buffer row of item i and its positions, fetched one item ahead.
+    auto pos_at = [&](int64_t row, int ax) -> int32_t {
+      return ax < 0 ? 0 : __ldg(p.pos + row * 3 + ax);
+    };
+    int64_t row_next = n_mine > 0 ? row_of(0) : 0;
+    int32_t pn0 = n_mine > 0 ? pos_at(row_next, ax0) : 0;
+    int32_t pn1 = n_mine > 0 ? pos_at(row_next, ax1) : 0;
     int64_t i = 0;
     bool ok = true;
     for (; i < n_mine; ++i) {
@@ -186,18 +214,21 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_con
         }
       }
       const uint32_t bar = full_bar + 8 * s;
+      const int64_t row = row_next;
       if (lane == 0) {
-        const int64_t g = first + i * step;
-        const int64_t row = g >> 1;
-        const int tt = static_cast<int>(g & 1);
+        stage_row[s] = row;
+        const int tt = static_cast<int>((first + i * step) & 1);
         mbar_arrive_expect_tx(bar, stage_bytes);
         bulk_load(sbase + s * stage_bytes, p.x[tt] + row * p.stride[tt], row_bytes, bar);
         if (kLora)
           bulk_load(sbase + s * stage_bytes + row_bytes, p.d[tt] + row * p.dstride[tt], row_bytes, bar);
       }
       const int32_t q0 = pn0, q1 = pn1;
-      pn0 = pos_of(i + 1, ax0);  // next row's positions, in flight meanwhile
-      pn1 = pos_of(i + 1, ax1);
+      if (i + 1 < n_mine) {  // next row's positions, in flight meanwhile
+        row_next = row_of(i + 1);
+        pn0 = pos_at(row_next, ax0);
+        pn1 = pos_at(row_next, ax1);
+      }
       float c0 = 1.0f, s0 = 0.0f, c1 = 1.0f, s1 = 0.0f;
       if (ax0 >= 0) sincosf(static_cast<float>(q0) * f0, &s0, &c0);
       if (ax1 >= 0) sincosf(static_cast<float>(q1) * f1, &s1, &c1);
@@ -223,7 +254,6 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_con
   for (int64_t i = 0; i < n_mine; ++i) {
     const int s = static_cast<int>(i % NST);
     const uint32_t parity = static_cast<uint32_t>((i / NST) & 1);
-    const int64_t row = (first + i * step) >> 1;
     const int tsel = static_cast<int>((first + i * step) & 1);
     // Wait for this row's bytes and table (bounded; uniform across the warp).
     bool ok = mbar_try_wait(full_bar + 8 * s, parity);
@@ -234,6 +264,7 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_con
         return;
       }
     }
+    const int64_t row = stage_row[s];
     float cs[8], sn[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -313,6 +344,7 @@ int prologue_max_heads(bool lora) {
 }
 
 cudaError_t launch_qk_norm_rope(const NormRopeArgs& a, cudaStream_t stream) {
+  if (a.n_seg < 1 || a.n_seg > kPrologueMaxSegments) return cudaErrorInvalidValue;
   NormRopeParams p{};
   p.x[0] = a.q;
   p.x[1] = a.k;
@@ -321,7 +353,6 @@ cudaError_t launch_qk_norm_rope(const NormRopeArgs& a, cudaStream_t stream) {
   p.w[0] = a.wq;
   p.w[1] = a.wk;
   p.pos = a.pos;
-  p.n_rows = a.n_rows;
   p.n_heads = a.n_heads;
   p.eps = a.eps;
   p.status = status_word_device_ptr();
@@ -355,7 +386,7 @@ cudaError_t launch_qk_norm_rope(const NormRopeArgs& a, cudaStream_t stream) {
   p.dstride[0] = a.dq_stride;
   p.dstride[1] = a.dk_stride;
   const size_t stage_bytes = (lora ? 2ull : 1ull) * a.n_heads * kHeadDim * 2;
-  auto smem_for = [&](int nst) { return nst * (stage_bytes + 64 * 8) + 2 * kMaxStages * 8; };
+  auto smem_for = [&](int nst) { return nst * (stage_bytes + 64 * 8) + 3 * kMaxStages * 8; };
   const int nst = smem_for(3) <= kMaxSmemPerBlock ? 3 : 2;
   p.n_stages = nst;
   const size_t smem = smem_for(nst);
@@ -383,8 +414,21 @@ cudaError_t launch_qk_norm_rope(const NormRopeArgs& a, cudaStream_t stream) {
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
+  // Valid rows are numbered across the segments; segments with no row are
+  // stepped over by the kernel.  The caller has checked that the total fits
+  // in int32 and that n_seg <= kPrologueMaxSegments.
+  int64_t total = 0;
+  for (int b = 0; b < a.n_seg; ++b) {
+    p.seg_cum[b] = static_cast<int32_t>(total);
+    p.seg_row0[b] = a.seg_row0[b];
+    total += a.seg_rows[b];
+  }
+  p.seg_cum[a.n_seg] = static_cast<int32_t>(total);
+  p.n_seg = a.n_seg;
+  p.n_rows = total;
+  if (total == 0) return cudaSuccess;
   int64_t grid = static_cast<int64_t>(sms) * per_sm;
-  if (grid > 2 * a.n_rows) grid = 2 * a.n_rows;
+  if (grid > 2 * total) grid = 2 * total;
   kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }

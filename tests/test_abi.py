@@ -71,6 +71,37 @@ def test_norm_rope_zero_rows_is_a_no_op(lib):
     assert norm_rope(lib, n=0, q=None, k=None) == H3_OK
 
 
+def norm_rope_varlen(lib, **kw):
+    a = dict(q=A, qs=5376, k=A + 0x100000, ks=5376, wq=A, wk=A, pos=A, cu=[0, 256, 512],
+             valid=[250, 256], n_seq=None, H=42, D=128, rt=32, rh=48, rw=48, theta=10000.0,
+             eps=1e-6, stream=None)
+    a.update(kw)
+    n_seq = a["n_seq"] if a["n_seq"] is not None else (len(a["cu"]) - 1 if a["cu"] else 1)
+    return lib.h3_qk_norm_rope_varlen(a["q"], a["qs"], a["k"], a["ks"], a["wq"], a["wk"], a["pos"],
+                                      _i32(a["cu"]) if a["cu"] is not None else None,
+                                      _i32(a["valid"]) if a["valid"] is not None else None,
+                                      n_seq, a["H"], a["D"], a["rt"], a["rh"], a["rw"],
+                                      a["theta"], a["eps"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n_seq=0), ARG), (dict(n_seq=17, cu=[0] * 18, valid=None), ARG), (dict(cu=None), ARG),
+    (dict(cu=[1, 256, 512]), ARG), (dict(cu=[0, 256, 100]), ARG), (dict(valid=[257, 0]), ARG),
+    (dict(valid=[0, -1]), ARG), (dict(H=0), ARG), (dict(D=64), SHAPE), (dict(rt=31), SHAPE),
+    (dict(qs=100), SHAPE), (dict(theta=0.0), ARG), (dict(eps=-1.0), ARG), (dict(k=A), ARG),
+    (dict(q=None), ARG), (dict(pos=None), ARG), (dict(q=A + 8), ALIGN), (dict(pos=A + 2), ALIGN),
+    (dict(ks=5377), ALIGN), (dict(cu=[0, 1 << 30, (1 << 30) + 2], valid=None), SHAPE),
+])
+def test_norm_rope_varlen_rejects_on_host(lib, kw, code):
+    assert norm_rope_varlen(lib, **kw) == code
+    assert lib.h3_last_error().decode() != ""
+
+
+def test_norm_rope_varlen_no_valid_row_is_a_no_op(lib):
+    assert norm_rope_varlen(lib, valid=[0, 0], q=None, k=None, pos=None) == H3_OK
+    assert norm_rope_varlen(lib, cu=[0, 0, 0], valid=None, q=None, k=None) == H3_OK
+
+
 def norm_rope_lora(lib, **kw):
     a = dict(q=A, qs=5376, dq=A + 0x200000, dqs=5376, k=A + 0x100000, ks=5376, dk=A + 0x300000,
              dks=5376, wq=A, wk=A, pos=A, n=10, H=42, D=128, rt=32, rh=48, rw=48, theta=10000.0,

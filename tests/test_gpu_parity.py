@@ -128,6 +128,58 @@ def test_prologue_head_counts(H, rows):
         prologue_bound(got, ref)
 
 
+VARLEN = {
+    # name: (heads, cu_seqlens, valid_len)
+    "two_ragged": (42, [0, 640, 1280], [611, 640]),
+    "empty_and_full": (5, [0, 384, 448, 576, 1216], [300, 0, 77, 640]),
+    "all_valid": (3, [0, 100, 357], None),
+    "sixteen_short": (2, list(range(0, 16 * 40 + 1, 40)), [40 - 2 * i for i in range(16)]),
+    "one_row_each": (7, [0, 1, 2, 3], [1, 1, 1]),
+}
+
+
+@pytest.mark.parametrize("case", sorted(VARLEN))
+def test_prologue_varlen(case):
+    """One launch over several packed sequences: bitwise the per-sequence
+    launches, within the prologue bound of the oracle, and no other row
+    (padding, or the rows past the last sequence) touched."""
+    H, cu, valid = VARLEN[case]
+    gen = torch.Generator().manual_seed(zlib.crc32(case.encode()))
+    R = cu[-1] + 64  # rows past the last sequence
+    q = torch.randn((R, H, 128), generator=gen).to(torch.bfloat16)
+    k = torch.randn((R, H, 128), generator=gen).to(torch.bfloat16)
+    wq = (1.0 + 0.1 * torch.randn((H, 128), generator=gen)).to(torch.bfloat16)
+    wk = (1.0 + 0.1 * torch.randn((H, 128), generator=gen)).to(torch.bfloat16)
+    pos = torch.randint(0, 1800, (R, 3), generator=gen, dtype=torch.int32)
+    n_valid = [valid[b] if valid is not None else cu[b + 1] - cu[b] for b in range(len(cu) - 1)]
+    for b, n in enumerate(n_valid):
+        q[cu[b] + n:cu[b + 1]] = float("nan")
+        k[cu[b] + n:cu[b + 1]] = float("inf")
+    q[cu[-1]:], k[cu[-1]:] = float("nan"), float("-inf")
+    dev = {n: t.cuda() for n, t in (("wq", wq), ("wk", wk), ("pos", pos))}
+    gq, gk = q.cuda(), k.cuda()
+    h3.qk_norm_rope_varlen(gq, gk, dev["wq"], dev["wk"], dev["pos"], cu, valid, rot=ROT)
+    sq, sk = q.cuda(), k.cuda()
+    for b, n in enumerate(n_valid):
+        if n:
+            h3.qk_norm_rope(sq[cu[b]:], sk[cu[b]:], dev["wq"], dev["wk"], dev["pos"][cu[b]:],
+                            n_rows=n, rot=ROT)
+    torch.cuda.synchronize()
+    for got, per_seq, src, w, t in ((gq, sq, q, wq, "q"), (gk, sk, k, wk, "k")):
+        got_bits = got.view(torch.int16).cpu()
+        assert torch.equal(got_bits, per_seq.view(torch.int16).cpu()), f"{t}: != per-sequence"
+        got64 = O.widen(got.cpu())
+        for b, n in enumerate(n_valid):
+            r0 = cu[b]
+            if n:
+                ref = O.qk_norm_rope(O.widen(src[r0:r0 + n]), O.widen(w), pos.numpy()[r0:r0 + n])
+                gate(got64[r0:r0 + n], ref, f"{case} {t} seq{b}")
+                prologue_bound(got64[r0:r0 + n], ref)
+            untouched = slice(r0 + n, cu[b + 1])
+            assert torch.equal(got_bits[untouched], src[untouched].view(torch.int16))
+        assert torch.equal(got_bits[cu[-1]:], src[cu[-1]:].view(torch.int16))
+
+
 @pytest.mark.parametrize("name", ["tiny", "medium"])
 def test_lora_prologue_matches_separate_branches_bitwise(name):
     # The pages' claim for the fused LoRA consumer: byte-exact against the
