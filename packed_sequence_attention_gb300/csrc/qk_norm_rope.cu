@@ -6,9 +6,11 @@
 // RoPE.  The point of the fusion is to read each wide activation once and
 // write it once, so the kernel is built around keeping HBM busy:
 //
-// * Persistent CTAs walk items g = blockIdx.x + i * gridDim.x; item g is
-//   valid row g / 2 of Q (g even) or of K (g odd): n_heads * 256 contiguous
-//   bytes.  Valid rows are numbered across the packed sequences of the
+// * Persistent CTAs walk items g = blockIdx.x + i * gridDim.x: items
+//   0 .. n-1 are the n valid rows of Q, items n .. 2n-1 those of K, each
+//   n_heads * 256 contiguous bytes.  All CTAs thus stream through Q, then
+//   through K, one address window at a time (interleaving Q and K rows put
+//   two windows in flight and was ~1 % slower).  Valid rows are numbered across the packed sequences of the
 //   launch (the valid rows of each, in order), so several sequences share one
 //   persistent grid and pay one tail.  The streaming warp holds the sequence
 //   table (at most 16 entries) in its lanes' registers, maps each item's valid
@@ -157,7 +159,7 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_con
 
   const int64_t first = blockIdx.x;
   const int64_t step = gridDim.x;
-  const int64_t n_items = 2 * p.n_rows;  // item g: valid row g >> 1, tensor g & 1
+  const int64_t n_items = 2 * p.n_rows;  // item g: Q row g, or K row g - n_rows
   const int64_t n_mine = first < n_items ? (n_items - 1 - first) / step + 1 : 0;
 
   if (tid == 0) {
@@ -189,14 +191,15 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_con
     const int32_t cum_l = lane < p.n_seg ? p.seg_cum[lane] : INT32_MAX;
     const int64_t row0_l = lane < p.n_seg ? p.seg_row0[lane] : 0;
     auto row_of = [&](int64_t i) -> int64_t {
-      const int64_t r = (first + i * step) >> 1;
+      const int64_t g = first + i * step;
+      const int64_t r = g >= p.n_rows ? g - p.n_rows : g;  // valid row of the item
       const int b = __popc(__ballot_sync(0xffffffffu, cum_l <= r)) - 1;
       return __shfl_sync(0xffffffffu, row0_l, b) + (r - __shfl_sync(0xffffffffu, cum_l, b));
     };
-    // Buffer row of item i and its positions, fetched one item ahead.
     auto pos_at = [&](int64_t row, int ax) -> int32_t {
       return ax < 0 ? 0 : __ldg(p.pos + row * 3 + ax);
     };
+    // Buffer row of the next item and its positions, fetched one item ahead.
     int64_t row_next = n_mine > 0 ? row_of(0) : 0;
     int32_t pn0 = n_mine > 0 ? pos_at(row_next, ax0) : 0;
     int32_t pn1 = n_mine > 0 ? pos_at(row_next, ax1) : 0;
@@ -217,7 +220,7 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_con
       const int64_t row = row_next;
       if (lane == 0) {
         stage_row[s] = row;
-        const int tt = static_cast<int>((first + i * step) & 1);
+        const int tt = (first + i * step) >= p.n_rows ? 1 : 0;
         mbar_arrive_expect_tx(bar, stage_bytes);
         bulk_load(sbase + s * stage_bytes, p.x[tt] + row * p.stride[tt], row_bytes, bar);
         if (kLora)
@@ -254,7 +257,7 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_con
   for (int64_t i = 0; i < n_mine; ++i) {
     const int s = static_cast<int>(i % NST);
     const uint32_t parity = static_cast<uint32_t>((i / NST) & 1);
-    const int tsel = static_cast<int>((first + i * step) & 1);
+    const int tsel = (first + i * step) >= p.n_rows ? 1 : 0;
     // Wait for this row's bytes and table (bounded; uniform across the warp).
     bool ok = mbar_try_wait(full_bar + 8 * s, parity);
     if (!__all_sync(0xffffffffu, ok)) {
