@@ -49,3 +49,28 @@ def test_rows_past_2_pow_31_elements():
     assert np.abs(got - ref).max() <= 2e-2
     assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 5e-3
     assert bool((out[:r0] == 0).all())  # the empty first sequence's rows are written as 0
+
+
+def test_varlen_prologue_rows_past_2_pow_31_elements():
+    # The same layout through the packed-sequence prologue: the second
+    # sequence's first buffer row comes from the launch's sequence table.
+    H, r0, n = 42, 400_000, 300
+    R = r0 + n + 16
+    gen = torch.Generator(device="cuda").manual_seed(32)
+    q, k = (torch.full((R, H, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+            for _ in range(2))
+    for t in (q, k):
+        t[r0:r0 + n] = torch.randn((n, H, 128), generator=gen, device="cuda").to(torch.bfloat16)
+    wq = (1 + 0.1 * torch.randn((H, 128), generator=gen, device="cuda")).to(torch.bfloat16)
+    wk = (1 + 0.1 * torch.randn((H, 128), generator=gen, device="cuda")).to(torch.bfloat16)
+    pos = torch.randint(0, 1800, (R, 3), generator=gen, device="cuda", dtype=torch.int32)
+    q_ref, k_ref = q[r0:r0 + n].clone(), k[r0:r0 + n].clone()
+    h3.qk_norm_rope(q_ref, k_ref, wq, wk, pos[r0:], n_rows=n)
+    h3.qk_norm_rope_varlen(q, k, wq, wk, pos, [0, r0, R], [0, n])
+    torch.cuda.synchronize()
+    fill = torch.full((1,), float("nan"), dtype=torch.bfloat16).view(torch.int16).item()
+    for got, ref in ((q, q_ref), (k, k_ref)):
+        assert torch.equal(got[r0:r0 + n].view(torch.int16), ref.view(torch.int16))
+        bits = got.view(torch.int16)
+        assert bool((bits[:r0] == fill).all())       # the empty sequence: untouched
+        assert bool((bits[r0 + n:] == fill).all())   # past the valid rows: untouched
