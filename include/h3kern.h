@@ -328,7 +328,8 @@ int h3_pack_qkv(const void* q, int64_t q_row_stride, const void* k, int64_t k_ro
                 int format, void* wire, h3_stream_t stream);
 
 /* wire [n_rows][n_heads_local] QKV records -> q, k, v [n_rows, n_heads_local, 128]
- * (INT8 values decoded and rounded to bf16). */
+ * (INT8 values decoded and rounded to bf16).  INT8 needs q, k, v and their
+ * row strides 16-byte aligned (H3_ERR_ALIGN otherwise). */
 int h3_unpack_qkv(const void* wire, int64_t n_rows, int n_heads_local, int format, void* q,
                   int64_t q_row_stride, void* k, int64_t k_row_stride, void* v,
                   int64_t v_row_stride, h3_stream_t stream);

@@ -593,6 +593,11 @@ int h3_unpack_qkv(const void* wire, int64_t n_rows, int n_heads_local, int forma
   if ((st = bf16_tensor(q, q_row_stride, w, "q")) || (st = bf16_tensor(k, k_row_stride, w, "k")) ||
       (st = bf16_tensor(v, v_row_stride, w, "v")))
     return st;
+  if (format == H3_WIRE_INT8 &&
+      (!aligned16(q) || !aligned16(k) || !aligned16(v) || (q_row_stride * 2) % 16 ||
+       (k_row_stride * 2) % 16 || (v_row_stride * 2) % 16))
+    return fail(H3_ERR_ALIGN, "INT8 unpacking writes 16-byte vectors: q, k, v and their row "
+                              "strides must be 16-byte aligned");
   if (!wire) return fail(H3_ERR_ARG, "wire is NULL");
   if (!aligned16(wire)) return fail(H3_ERR_ALIGN, "wire must be 16-byte aligned");
   if (n_rows == 0) return H3_OK;

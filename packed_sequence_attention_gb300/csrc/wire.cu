@@ -351,32 +351,21 @@ __global__ void __launch_bounds__(kInt8Warps * 32, 4) pack_qkv_int8_kernel(
   }
 }
 
-// Records of one part are [rows][hl], so unit u is record u.
-template <int kFmt>
-__global__ void __launch_bounds__(kWarps * 32) unpack_qkv_kernel(
+// BF16 QKV unpack.  Records of one part are [rows][hl], so unit u is record u.
+__global__ void __launch_bounds__(kWarps * 32) unpack_qkv_bf16_kernel(
     const uint8_t* __restrict__ wire, int64_t n_rows, int hl, __nv_bfloat16* __restrict__ q,
     int64_t qs, __nv_bfloat16* __restrict__ k, int64_t ks, __nv_bfloat16* __restrict__ v,
     int64_t vs) {
   constexpr int kU = 2;
-  constexpr int kRec = kFmt == H3_WIRE_BF16 ? 768 : 400;
   const int lane = threadIdx.x & 31;
   const Units<kU> un(n_rows * hl, hl);
   uint2 in[kU][3];
-  uint32_t codes[kU][3];
 #pragma unroll
   for (int u = 0; u < kU; ++u) {
     if (un.ok[u]) {
-      const uint8_t* src = wire + (un.r[u] * hl + un.h[u]) * kRec;
-      if (kFmt == H3_WIRE_BF16) {
+      const uint8_t* src = wire + (un.r[u] * hl + un.h[u]) * 768;
 #pragma unroll
-        for (int t = 0; t < 3; ++t) in[u][t] = ld8(src + t * 256 + lane * 8);
-      } else {
-#pragma unroll
-        for (int t = 0; t < 3; ++t) {
-          in[u][t].x = __ldg(reinterpret_cast<const uint32_t*>(src + t * 128 + lane * 4));
-          codes[u][t] = src[384 + t * 4 + (lane >> 3)];
-        }
-      }
+      for (int t = 0; t < 3; ++t) in[u][t] = ld8(src + t * 256 + lane * 8);
     }
   }
 #pragma unroll
@@ -385,9 +374,73 @@ __global__ void __launch_bounds__(kWarps * 32) unpack_qkv_kernel(
     const int64_t c = un.h[u] * kHeadDim + lane * 4;
     __nv_bfloat16* dst[3] = {q + un.r[u] * qs + c, k + un.r[u] * ks + c, v + un.r[u] * vs + c};
 #pragma unroll
-    for (int t = 0; t < 3; ++t)
-      *reinterpret_cast<uint2*>(dst[t]) =
-          kFmt == H3_WIRE_BF16 ? in[u][t] : dequant4(in[u][t].x, codes[u][t]);
+    for (int t = 0; t < 3; ++t) *reinterpret_cast<uint2*>(dst[t]) = in[u][t];
+  }
+}
+
+// Block-INT8 QKV unpack.  A quarter-warp decodes one tensor row (the 128
+// values of q, k or v of one record) per pass; lane s of the quarter owns
+// channels 8s .. 8s+7 and 64+8s .. 64+8s+7, so that each of its two 16-byte
+// stores covers, across the quarter, 128 contiguous bytes (whole sectors),
+// and each of its two 8-byte loads 64 contiguous bytes; one 4-byte load
+// brings the tensor's four scale codes.  Tensor rows are numbered
+// f = 3 * record + tensor, and the grid's warp count is a multiple of 3, so a
+// quarter-warp that advances by 4 * warps keeps its tensor and moves its
+// (row, head) by constants with a carry, without dividing.  The next pass's
+// bytes are loaded before the current ones are decoded.
+constexpr int kUnpackWarps = 8;
+
+__global__ void __launch_bounds__(kUnpackWarps * 32) unpack_qkv_int8_kernel(
+    const uint8_t* __restrict__ wire, uint32_t n_rec, uint32_t hl, __nv_bfloat16* __restrict__ q,
+    int64_t qs, __nv_bfloat16* __restrict__ k, int64_t ks, __nv_bfloat16* __restrict__ v,
+    int64_t vs) {
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & 7;
+  const uint32_t f0 = (blockIdx.x * kUnpackWarps + (threadIdx.x >> 5)) * 4 + (lane >> 3);
+  const int t = static_cast<int>(f0 % 3);
+  const uint32_t du = gridDim.x * kUnpackWarps / 3 * 4;  // records per pass
+  const uint32_t du_row = du / hl, du_head = du - du_row * hl;
+  uint32_t u = f0 / 3;
+  uint32_t row = u / hl, head = u - row * hl;
+  __nv_bfloat16* const base = t == 0 ? q : (t == 1 ? k : v);
+  const int64_t stride = t == 0 ? qs : (t == 1 ? ks : vs);
+  const uint32_t off = t * 128 + sub * 8;  // value bytes of channels 8s.. (and 64 + 8s.. at +64)
+  const int g0 = sub >> 2;                 // 32-channel groups of the two chunks: g0 and g0 + 2
+  uint2 b0 = make_uint2(0u, 0u), b1 = b0;
+  uint32_t codes = 0u;
+  if (u < n_rec) {
+    const uint8_t* rec = wire + static_cast<size_t>(u) * 400;
+    b0 = __ldg(reinterpret_cast<const uint2*>(rec + off));
+    b1 = __ldg(reinterpret_cast<const uint2*>(rec + off + 64));
+    codes = __ldg(reinterpret_cast<const uint32_t*>(rec + 384 + t * 4));
+  }
+  while (u < n_rec) {
+    const uint32_t un = u + du;  // < 2^32: both terms are below 2^31
+    uint2 n0 = b0, n1 = b1;
+    uint32_t nc = codes;
+    if (un < n_rec) {
+      const uint8_t* rec = wire + static_cast<size_t>(un) * 400;
+      n0 = __ldg(reinterpret_cast<const uint2*>(rec + off));
+      n1 = __ldg(reinterpret_cast<const uint2*>(rec + off + 64));
+      nc = __ldg(reinterpret_cast<const uint32_t*>(rec + 384 + t * 4));
+    }
+    const int c0 = static_cast<int>((codes >> (8 * g0)) & 0xFFu);
+    const int c1 = static_cast<int>((codes >> (8 * (g0 + 2))) & 0xFFu);
+    const uint2 o0 = dequant4(b0.x, c0), o1 = dequant4(b0.y, c0);
+    const uint2 o2 = dequant4(b1.x, c1), o3 = dequant4(b1.y, c1);
+    __nv_bfloat16* dst = base + static_cast<int64_t>(row) * stride + head * kHeadDim + sub * 8;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(o0.x, o0.y, o1.x, o1.y);
+    *reinterpret_cast<uint4*>(dst + 64) = make_uint4(o2.x, o2.y, o3.x, o3.y);
+    u = un;
+    b0 = n0;
+    b1 = n1;
+    codes = nc;
+    head += du_head;
+    row += du_row;
+    if (head >= hl) {
+      head -= hl;
+      ++row;
+    }
   }
 }
 
@@ -525,13 +578,38 @@ cudaError_t launch_pack_qkv(const WireQkvArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_unpack_qkv(const WireQkvArgs& a, cudaStream_t s) {
-  const unsigned g = blocks_for(a.n_rows * a.n_heads, 2);
-  if (a.format == H3_WIRE_BF16)
-    unpack_qkv_kernel<H3_WIRE_BF16><<<g, kWarps * 32, 0, s>>>(a.wire, a.n_rows, a.n_heads, a.qm,
-                                                              a.qs, a.km, a.ks, a.vm, a.vs);
-  else
-    unpack_qkv_kernel<H3_WIRE_INT8><<<g, kWarps * 32, 0, s>>>(a.wire, a.n_rows, a.n_heads, a.qm,
-                                                              a.qs, a.km, a.ks, a.vm, a.vs);
+  if (a.format == H3_WIRE_BF16) {
+    const unsigned g = blocks_for(a.n_rows * a.n_heads, 2);
+    unpack_qkv_bf16_kernel<<<g, kWarps * 32, 0, s>>>(a.wire, a.n_rows, a.n_heads, a.qm, a.qs,
+                                                     a.km, a.ks, a.vm, a.vs);
+    return cudaGetLastError();
+  }
+  // Block-INT8: persistent, as many blocks as fit at once (or fewer for a
+  // small input), rounded to a multiple of 3 blocks (see the kernel).
+  static std::atomic<int64_t> full_cache[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int64_t full = full_cache[dev].load();
+  if (full == 0) {
+    int per_sm = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, unpack_qkv_int8_kernel,
+                                                      kUnpackWarps * 32, 0);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    full = static_cast<int64_t>(sms) * (per_sm < 1 ? 1 : per_sm) / 3 * 3;
+    if (full < 3) full = 3;
+    full_cache[dev].store(full);
+  }
+  const int64_t rows_of_tensors = 3 * a.n_rows * a.n_heads;      // q, k and v of every record
+  int64_t need = (rows_of_tensors + kUnpackWarps * 4 - 1) / (kUnpackWarps * 4);
+  need = (need + 2) / 3 * 3;
+  const unsigned g = static_cast<unsigned>(need < full ? need : full);
+  unpack_qkv_int8_kernel<<<g, kUnpackWarps * 32, 0, s>>>(
+      a.wire, static_cast<uint32_t>(a.n_rows * a.n_heads), static_cast<uint32_t>(a.n_heads), a.qm,
+      a.qs, a.km, a.ks, a.vm, a.vs);
   return cudaGetLastError();
 }
 

@@ -255,6 +255,31 @@ def test_pack_qkv_bf16_allows_8_byte_alignment(lib):
     assert st in (DEVICE, ARCH) or (torch.cuda.is_available() and st == ARG)
 
 
+def unpack_qkv(lib, **kw):
+    a = dict(wire=A, n=10, hl=21, fmt=1, q=A, qs=2688, k=A + 0x100000, ks=2688, v=A + 0x200000,
+             vs=2688)
+    a.update(kw)
+    return lib.h3_unpack_qkv(a["wire"], a["n"], a["hl"], a["fmt"], a["q"], a["qs"], a["k"], a["ks"],
+                             a["v"], a["vs"], None)
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(fmt=2), ARG), (dict(wire=None), ARG), (dict(wire=A + 8), ALIGN), (dict(qs=100), SHAPE),
+    (dict(q=A + 8), ALIGN), (dict(ks=2688 + 4), ALIGN), (dict(v=A + 4), ALIGN),
+])
+def test_unpack_qkv_int8_rejects_on_host(lib, args, code):
+    assert unpack_qkv(lib, **args) == code
+
+
+def test_unpack_qkv_bf16_allows_8_byte_alignment(lib):
+    """BF16 records move 8-byte vectors: 8-byte aligned outputs pass the host
+    checks (and, without a GPU, stop at the device check); INT8 writes 16-byte
+    vectors and needs 16-byte alignment."""
+    st = unpack_qkv(lib, fmt=0, q=A + 8, qs=2688 + 4)
+    assert st in (DEVICE, ARCH) or (torch.cuda.is_available() and st == ARG)
+    assert unpack_qkv(lib, fmt=1, q=A + 8, qs=2688 + 4) == ALIGN
+
+
 @pytest.mark.parametrize("args,code", [
     (dict(ns=5), ARG), (dict(fmt=3), ARG), (dict(o=None), ARG), (dict(os_=100), SHAPE),
     (dict(wire=None), ARG), (dict(wire=A + 4), ALIGN), (dict(n=2 ** 33), ARG),
