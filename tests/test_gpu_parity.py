@@ -83,7 +83,13 @@ def test_prologue_full_compare(name):
     inp = W.make_inputs(name)
     g = to_dev(inp)
     run_prologue(g)
+    # the one-launch form the bench step and attention_block use: the same bits
+    qv, kv = inp["q"].cuda(), inp["k"].cuda()
+    h3.qk_norm_rope_varlen(qv, kv, g["wq"], g["wk"], g["pos_thw"], g["cu_seqlens_q"],
+                           g["valid_len"], rot=ROT)
     torch.cuda.synchronize()
+    assert torch.equal(qv.view(torch.int16), g["q"].view(torch.int16))
+    assert torch.equal(kv.view(torch.int16), g["k"].view(torch.int16))
     w = inp["workload"]
     pos = inp["pos_thw"].numpy()
     for t, wn in (("q", "wq"), ("k", "wk")):
