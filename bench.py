@@ -440,7 +440,7 @@ def bench_gpu(args):
 def rmw_ceiling(g, w, stream, iters=10):
     """torch's own in-place read-modify-write (x *= 1, which changes no bit)
     over the valid Q and K rows the prologue reads and writes: the rate a
-    plain streaming kernel reaches on this machine, in this run."""
+    plain streaming kernel reaches on this GPU, in this run."""
     views = []
     for b, s in enumerate(w.segments):
         if s.n_valid_q():
