@@ -36,12 +36,11 @@ import torch
 
 from . import _binding
 
-__all__ = ["H3Error", "qk_norm_rope", "qk_norm_rope_varlen", "qk_norm_rope_lora", "attention", "attention_groups",
-           "block_means", "block_means_qk", "block_select", "sparse_attention", "sol_attention",
-           "WIRE_BF16", "WIRE_INT8", "WIRE_FP8", "wire_record_bytes", "pack_qkv", "unpack_qkv",
-           "pack_out", "merge_heads",
-           "status_word", "lib", "HEAD_DIM", "MAX_SEGMENTS", "attention_block",
-           "copy_2d", "head_groups", "HostPipeline"]
+__all__ = ["H3Error", "qk_norm_rope", "qk_norm_rope_varlen", "qk_norm_rope_lora", "attention",
+           "attention_groups", "block_means", "block_means_qk", "block_select", "sparse_attention",
+           "sol_attention", "WIRE_BF16", "WIRE_INT8", "WIRE_FP8", "wire_record_bytes", "pack_qkv",
+           "unpack_qkv", "pack_out", "merge_heads", "status_word", "lib", "HEAD_DIM",
+           "MAX_SEGMENTS", "attention_block", "copy_2d", "head_groups", "HostPipeline"]
 
 HEAD_DIM = 128
 MAX_SEGMENTS = 16
